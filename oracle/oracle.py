@@ -1,0 +1,198 @@
+"""ctypes wrapper around oracle.c (plain fp64 C, OpenMP over items).
+
+TEST INFRASTRUCTURE ONLY.  The oracle restates, from the torch-projectors paper
+summaries (gist.science: Method section bullets on the RFFT half-spectrum format,
+linear / Catmull-Rom interpolation, Friedel symmetry, the four projection operations,
+shifts by phase modulation and gradients for inputs, rotations and shifts), what the
+projection computes, one pixel and one tap at a time.  It shares no code with the CUDA
+library and is never called by it.
+
+Every wrapper takes numpy arrays (any float dtype; they are widened to fp64 /
+complex128) and returns fresh numpy arrays.  ``nthreads`` defaults to every core this
+process may run on.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+from pathlib import Path
+
+import numpy as np
+
+LINEAR, CUBIC = 0, 1
+FFTW, CENTERED = 0, 1
+
+_HERE = Path(__file__).resolve().parent
+_SRC = _HERE / "oracle.c"
+_LIB = _HERE / "liboracle.so"
+_lib = None
+
+
+def build(force: bool = False) -> Path:
+    """Compile oracle.c into liboracle.so (gcc, -O2, no fast-math, no FMA contraction)."""
+    if force or not _LIB.exists() or _LIB.stat().st_mtime < _SRC.stat().st_mtime:
+        tmp = _LIB.with_suffix(f".so.{os.getpid()}")
+        subprocess.run(
+            ["gcc", "-std=gnu11", "-O2", "-ffp-contract=off", "-fopenmp", "-fPIC", "-shared",
+             "-o", str(tmp), str(_SRC), "-lm"],
+            check=True,
+        )
+        os.replace(tmp, _LIB)
+    return _LIB
+
+
+def _load():
+    global _lib
+    if _lib is None:
+        # TP_ORACLE_LIB points the wrapper at another build of oracle.c; the mutation
+        # tests use it to check that the pins reject deliberately broken oracles.
+        alt = os.environ.get("TP_ORACLE_LIB")
+        if not alt:
+            build()
+        lib = ctypes.CDLL(alt or str(_LIB))
+        P, I, D, L = ctypes.c_void_p, ctypes.c_int, ctypes.c_double, ctypes.c_long
+        lib.orc_project.argtypes = [I, P, I, I, P, I, I, P, I, P, I, I, I, D, D, I]
+        lib.orc_project_samples.argtypes = [I, P, I, I, P, I, I, P, I, I, I, I, D, D, L, P, P, P, I]
+        lib.orc_backproject.argtypes = [I, P, P, I, I, P, I, I, P, I, P, P, I, I, I, D, D, I]
+        lib.orc_project_backward.argtypes = [I, P, I, I, P, I, I, P, I, P, I, P, P, P, I, I, D, D, I]
+        lib.orc_axis_weights.argtypes = [D, I, P, P, P]
+        for f in (lib.orc_project, lib.orc_project_samples, lib.orc_backproject,
+                  lib.orc_project_backward, lib.orc_axis_weights):
+            f.restype = I
+        _lib = lib
+    return _lib
+
+
+def _cores() -> int:
+    try:
+        return len(os.sched_getaffinity(0))
+    except AttributeError:  # pragma: no cover
+        return os.cpu_count() or 1
+
+
+def _c128(a):
+    return np.ascontiguousarray(a, dtype=np.complex128)
+
+
+def _f64(a):
+    return np.ascontiguousarray(a, dtype=np.float64)
+
+
+def _ptr(a):
+    return None if a is None else a.ctypes.data_as(ctypes.c_void_p)
+
+
+def _check(rc: int, what: str):
+    if rc != 0:
+        raise ValueError(f"oracle {what} rejected its arguments (code {rc})")
+
+
+def _dims(ndim, rec_shape, rot, shift):
+    n_rec = rec_shape[0]
+    Dv = rec_shape[1]
+    k = ndim
+    rot = _f64(rot)
+    if rot.ndim != 4 or rot.shape[2:] != (k, k):
+        raise ValueError("rot must be [n_rot][n_pose][k][k]")
+    n_rot, n_pose = rot.shape[:2]
+    n_sh = 1
+    if shift is not None:
+        shift = _f64(shift)
+        if shift.ndim != 3 or shift.shape[1:] != (n_pose, 2):
+            raise ValueError("shift must be [n_sh][n_pose][2]")
+        n_sh = shift.shape[0]
+    return n_rec, Dv, rot, n_rot, n_pose, shift, n_sh
+
+
+def project(ndim, rec, rot, shift=None, Do=None, interp=CUBIC, layout=CENTERED,
+            oversampling=1.0, cutoff=-1.0, nthreads=None):
+    """Forward projection: [n_rec][n_pose][Do][Do/2+1] complex128."""
+    rec = _c128(rec)
+    n_rec, Dv, rot, n_rot, n_pose, shift, n_sh = _dims(ndim, rec.shape, rot, shift)
+    Do = Dv if Do is None else Do
+    out = np.zeros((n_rec, n_pose, Do, Do // 2 + 1), np.complex128)
+    rc = _load().orc_project(ndim, _ptr(rec), n_rec, Dv, _ptr(rot), n_rot, n_pose, _ptr(shift),
+                             n_sh, _ptr(out), Do, interp, layout, oversampling, cutoff,
+                             nthreads or _cores())
+    _check(rc, "project")
+    return out
+
+
+def project_samples(ndim, rec, rot, items, pix, shift=None, Do=None, interp=CUBIC,
+                    layout=CENTERED, oversampling=1.0, cutoff=-1.0, nthreads=None):
+    """Forward projection at (item, pixel) pairs only; item = r*n_pose + p, pix = i*H + j."""
+    rec = _c128(rec)
+    n_rec, Dv, rot, n_rot, n_pose, shift, n_sh = _dims(ndim, rec.shape, rot, shift)
+    Do = Dv if Do is None else Do
+    items = np.ascontiguousarray(items, dtype=np.int64)
+    pix = np.ascontiguousarray(pix, dtype=np.int64)
+    vals = np.zeros(items.shape[0], np.complex128)
+    rc = _load().orc_project_samples(ndim, _ptr(rec), n_rec, Dv, _ptr(rot), n_rot, n_pose,
+                                     _ptr(shift), n_sh, Do, interp, layout, oversampling, cutoff,
+                                     items.shape[0], _ptr(items), _ptr(pix), _ptr(vals),
+                                     nthreads or _cores())
+    _check(rc, "project_samples")
+    return vals
+
+
+def backproject(ndim, proj, rot, weights=None, shift=None, Dv=None, interp=CUBIC,
+                layout=CENTERED, oversampling=1.0, cutoff=-1.0, nthreads=None,
+                want_weights=True):
+    """Back-projection (insertion): returns (rec [n_rec][...] complex128, wrec float64 or None)."""
+    proj = _c128(proj)
+    n_rec, n_pose_p, Do = proj.shape[0], proj.shape[1], proj.shape[2]
+    rot = _f64(rot)
+    k = ndim
+    n_rot, n_pose = rot.shape[:2]
+    if n_pose != n_pose_p:
+        raise ValueError("rot and proj disagree on n_pose")
+    n_sh = 1
+    if shift is not None:
+        shift = _f64(shift)
+        n_sh = shift.shape[0]
+    if weights is not None:
+        weights = _f64(weights)
+        if weights.shape != proj.shape:
+            raise ValueError("weights must have the projection shape")
+    Dv = Do if Dv is None else Dv
+    H = Dv // 2 + 1
+    shape = (n_rec, Dv, Dv, H) if ndim == 3 else (n_rec, Dv, H)
+    rec = np.zeros(shape, np.complex128)
+    wrec = np.zeros(shape, np.float64) if want_weights else None
+    rc = _load().orc_backproject(ndim, _ptr(proj), _ptr(weights), n_rec, Do, _ptr(rot), n_rot,
+                                 n_pose, _ptr(shift), n_sh, _ptr(rec), _ptr(wrec), Dv, interp,
+                                 layout, oversampling, cutoff, nthreads or _cores())
+    _check(rc, "backproject")
+    assert rot.shape[2:] == (k, k)
+    return rec, wrec
+
+
+def project_backward(ndim, rec, rot, grad_out, shift=None, interp=CUBIC, layout=CENTERED,
+                     oversampling=1.0, cutoff=-1.0, nthreads=None, want_rec=True,
+                     want_rot=True, want_shift=True):
+    """Backward of project(): (grad_rec, grad_rot, grad_shift); unwanted ones are None."""
+    rec = _c128(rec)
+    n_rec, Dv, rot, n_rot, n_pose, shift, n_sh = _dims(ndim, rec.shape, rot, shift)
+    grad_out = _c128(grad_out)
+    Do = grad_out.shape[2]
+    if grad_out.shape != (n_rec, n_pose, Do, Do // 2 + 1):
+        raise ValueError("grad_out must be [n_rec][n_pose][Do][Do/2+1]")
+    g_rec = np.zeros(rec.shape, np.complex128) if want_rec else None
+    g_rot = np.zeros(rot.shape, np.float64) if want_rot else None
+    g_sh = np.zeros((n_sh, n_pose, 2), np.float64) if want_shift else None
+    rc = _load().orc_project_backward(ndim, _ptr(rec), n_rec, Dv, _ptr(rot), n_rot, n_pose,
+                                      _ptr(shift), n_sh, _ptr(grad_out), Do, _ptr(g_rec),
+                                      _ptr(g_rot), _ptr(g_sh), interp, layout, oversampling,
+                                      cutoff, nthreads or _cores())
+    _check(rc, "project_backward")
+    return g_rec, g_rot, g_sh
+
+
+def axis_weights(c: float, interp=CUBIC):
+    """Taps, kernel weights and kernel derivatives of one axis at coordinate c."""
+    t = np.zeros(4, np.int64)
+    w = np.zeros(4, np.float64)
+    dw = np.zeros(4, np.float64)
+    n = _load().orc_axis_weights(float(c), interp, _ptr(t), _ptr(w), _ptr(dw))
+    return t[:n], w[:n], dw[:n]
