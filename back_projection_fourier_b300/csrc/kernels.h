@@ -1,0 +1,25 @@
+// kernels.h -- internal launchers of libtp.so (C++ only; the public ABI is include/tp.h).
+#pragma once
+
+#include <cuda_runtime.h>
+
+#include "tp_device.cuh"
+
+namespace tp {
+
+// Each launcher enqueues on `stream` and returns cudaGetLastError().  Arguments have been
+// validated by the ABI layer; `sms` is the device's SM count (grid sizing).
+cudaError_t launch_project(int ndim, int interp, const Geom& g, const void* rec,
+                           const float* rot, const float* shift, void* out, int sms,
+                           cudaStream_t stream);
+
+cudaError_t launch_backward(int ndim, int interp, const Geom& g, const void* rec,
+                            const float* rot, const float* shift, const void* grad_out,
+                            void* grad_rec, float* grad_rot, float* grad_shift, int sms,
+                            cudaStream_t stream);
+
+cudaError_t launch_backproject(int ndim, int interp, const Geom& g, const void* proj,
+                               const float* weights, const float* rot, const float* shift,
+                               void* vol_out, float* wvol_out, int sms, cudaStream_t stream);
+
+}  // namespace tp

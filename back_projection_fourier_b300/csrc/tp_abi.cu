@@ -1,0 +1,234 @@
+// tp_abi.cu -- the extern "C" entry points of libtp.so declared in include/tp.h:
+// argument validation on the host, derived geometry, output zeroing and the launches.
+#include <cmath>
+#include <cstdint>
+#include <climits>
+
+#include "../../include/tp.h"
+#include "kernels.h"
+
+namespace {
+
+constexpr int kMaxBox3 = 1024;
+constexpr int kMaxBox2 = 32768;
+
+struct Opts {
+    int interp = TP_CUBIC;
+    int layout = TP_LAYOUT_CENTERED;
+    float o = 1.0f;
+    float cutoff = -1.0f;
+};
+
+tp_status read_opts(const tp_opts* in, Opts& o)
+{
+    if (in) {
+        o.interp = in->interp;
+        o.layout = in->layout;
+        o.o = in->oversampling;
+        o.cutoff = in->cutoff;
+    }
+    if (o.interp != TP_LINEAR && o.interp != TP_CUBIC) return TP_ERR_VALUE;
+    if (o.layout != TP_LAYOUT_FFTW && o.layout != TP_LAYOUT_CENTERED) return TP_ERR_VALUE;
+    if (!(o.o > 0.0f) || !std::isfinite(o.o)) return TP_ERR_VALUE;
+    if (!std::isfinite(o.cutoff)) return TP_ERR_VALUE;
+    return TP_OK;
+}
+
+bool box_ok(int D, int ndim)
+{
+    return D >= 2 && (D % 2) == 0 && D <= (ndim == 3 ? kMaxBox3 : kMaxBox2);
+}
+
+bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+// Shapes shared by every call.  `need_*` says whether the pointer is required.
+tp_status check_common(int ndim, int n_rec, int Dv, int Do, int n_rot, int n_pose,
+                       const float* shift, int n_sh)
+{
+    if (ndim != 2 && ndim != 3) return TP_ERR_VALUE;
+    if (n_rec < 0 || n_pose < 0) return TP_ERR_SHAPE;
+    if (!box_ok(Dv, ndim) || !box_ok(Do, ndim)) return TP_ERR_SHAPE;
+    if (n_rot != 1 && n_rot != n_rec) return TP_ERR_SHAPE;
+    if (shift && n_sh != 1 && n_sh != n_rec) return TP_ERR_SHAPE;
+    return TP_OK;
+}
+
+tp::Geom make_geom(int ndim, int n_rec, int Dv, int n_rot, int n_pose, const float* shift,
+                   int n_sh, int Do, const Opts& o)
+{
+    tp::Geom g;
+    g.n_rec = n_rec;
+    g.n_pose = n_pose;
+    g.rot_shared = n_rot == 1;
+    g.sh_shared = n_sh == 1;
+    g.Dv = Dv;
+    g.Hv = Dv / 2 + 1;
+    g.halfv = Dv / 2;
+    g.Do = Do;
+    g.Ho = Do / 2 + 1;
+    g.halfo = Do / 2;
+    g.centered = o.layout == TP_LAYOUT_CENTERED;
+    g.has_shift = shift != nullptr;
+    g.o_is_one = o.o == 1.0f;
+    g.o = o.o;
+    g.Do_f = (float)Do;
+    g.inv_Do = 1.0f / (float)Do;
+    // kx^2 + ky^2 <= rc^2  <=>  kx^2 + ky^2 <= floor(rc^2) for integer kx, ky; rc^2 of an
+    // fp32 rc is exact in double.
+    const double rc = o.cutoff < 0.0f ? 0.5 * Do : (double)o.cutoff;
+    const double rc2 = std::floor(rc * rc);
+    g.rc2 = rc2 >= (double)INT_MAX ? INT_MAX : (int)rc2;
+    g.rec_elems = ndim == 3 ? (long long)Dv * Dv * g.Hv : (long long)Dv * g.Hv;
+    g.img_elems = (long long)Do * g.Ho;
+    return g;
+}
+
+int sm_count()
+{
+    int dev = 0, sms = 148;
+    if (cudaGetDevice(&dev) == cudaSuccess)
+        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    return sms > 0 ? sms : 148;
+}
+
+tp_status project_impl(int ndim, const void* rec, int n_rec, int Dv, const float* rot,
+                       int n_rot, int n_pose, const float* shift, int n_sh, void* out, int Do,
+                       const tp_opts* opts, void* stream)
+{
+    Opts o;
+    tp_status st = read_opts(opts, o);
+    if (st != TP_OK) return st;
+    st = check_common(ndim, n_rec, Dv, Do, n_rot, n_pose, shift, n_sh);
+    if (st != TP_OK) return st;
+    const long long n_items = (long long)n_rec * n_pose;
+    if (n_items == 0) return TP_OK;
+    if (!rec || !rot || !out) return TP_ERR_NULL;
+    if (!aligned(rec, 8) || !aligned(out, 8) || !aligned(rot, 4) || (shift && !aligned(shift, 4)))
+        return TP_ERR_VALUE;
+    const tp::Geom g = make_geom(ndim, n_rec, Dv, n_rot, n_pose, shift, n_sh, Do, o);
+    const cudaError_t e = tp::launch_project(ndim, o.interp, g, rec, rot, shift, out, sm_count(),
+                                             static_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? TP_OK : TP_ERR_CUDA;
+}
+
+tp_status backproject_impl(int ndim, const void* proj, const float* weights, int n_rec, int Do,
+                           const float* rot, int n_rot, int n_pose, const float* shift, int n_sh,
+                           void* vol_out, float* wvol_out, int Dv, int accumulate,
+                           const tp_opts* opts, void* stream)
+{
+    Opts o;
+    tp_status st = read_opts(opts, o);
+    if (st != TP_OK) return st;
+    st = check_common(ndim, n_rec, Dv, Do, n_rot, n_pose, shift, n_sh);
+    if (st != TP_OK) return st;
+    if (accumulate != 0 && accumulate != 1) return TP_ERR_VALUE;
+    const long long n_items = (long long)n_rec * n_pose;
+    if (n_rec > 0 && !vol_out && !wvol_out) return TP_OK;
+    if (n_items > 0) {
+        if (!rot || (vol_out && !proj)) return TP_ERR_NULL;
+        if ((proj && !aligned(proj, 8)) || (weights && !aligned(weights, 4)) || !aligned(rot, 4) ||
+            (shift && !aligned(shift, 4)))
+            return TP_ERR_VALUE;
+    }
+    if ((vol_out && !aligned(vol_out, 8)) || (wvol_out && !aligned(wvol_out, 4)))
+        return TP_ERR_VALUE;
+    const tp::Geom g = make_geom(ndim, n_rec, Dv, n_rot, n_pose, shift, n_sh, Do, o);
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if (!accumulate && n_rec > 0) {
+        const size_t elems = (size_t)g.rec_elems * (size_t)n_rec;
+        if (vol_out && cudaMemsetAsync(vol_out, 0, elems * 8, s) != cudaSuccess) return TP_ERR_CUDA;
+        if (wvol_out && cudaMemsetAsync(wvol_out, 0, elems * 4, s) != cudaSuccess) return TP_ERR_CUDA;
+    }
+    if (n_items == 0) return TP_OK;
+    const cudaError_t e = tp::launch_backproject(ndim, o.interp, g, proj, weights, rot, shift,
+                                                 vol_out, wvol_out, sm_count(), s);
+    return e == cudaSuccess ? TP_OK : TP_ERR_CUDA;
+}
+
+}  // namespace
+
+extern "C" {
+
+tp_status tp_project_3d_to_2d(const void* vol, int n_rec, int Dv, const float* rot, int n_rot,
+                              int n_pose, const float* shift, int n_sh, void* out, int Do,
+                              const tp_opts* opts, void* stream)
+{
+    return project_impl(3, vol, n_rec, Dv, rot, n_rot, n_pose, shift, n_sh, out, Do, opts, stream);
+}
+
+tp_status tp_project_2d_to_2d(const void* img, int n_rec, int Dv, const float* rot, int n_rot,
+                              int n_pose, const float* shift, int n_sh, void* out, int Do,
+                              const tp_opts* opts, void* stream)
+{
+    return project_impl(2, img, n_rec, Dv, rot, n_rot, n_pose, shift, n_sh, out, Do, opts, stream);
+}
+
+tp_status tp_backproject_2d_to_3d(const void* proj, const float* weights, int n_rec, int Do,
+                                  const float* rot, int n_rot, int n_pose, const float* shift,
+                                  int n_sh, void* vol_out, float* wvol_out, int Dv,
+                                  int accumulate, const tp_opts* opts, void* stream)
+{
+    return backproject_impl(3, proj, weights, n_rec, Do, rot, n_rot, n_pose, shift, n_sh, vol_out,
+                            wvol_out, Dv, accumulate, opts, stream);
+}
+
+tp_status tp_backproject_2d_to_2d(const void* proj, const float* weights, int n_rec, int Do,
+                                  const float* rot, int n_rot, int n_pose, const float* shift,
+                                  int n_sh, void* img_out, float* wimg_out, int Dv,
+                                  int accumulate, const tp_opts* opts, void* stream)
+{
+    return backproject_impl(2, proj, weights, n_rec, Do, rot, n_rot, n_pose, shift, n_sh, img_out,
+                            wimg_out, Dv, accumulate, opts, stream);
+}
+
+tp_status tp_project_backward(int ndim, const void* rec, int n_rec, int Dv, const float* rot,
+                              int n_rot, int n_pose, const float* shift, int n_sh,
+                              const void* grad_out, int Do, void* grad_rec, float* grad_rot,
+                              float* grad_shift, const tp_opts* opts, void* stream)
+{
+    Opts o;
+    tp_status st = read_opts(opts, o);
+    if (st != TP_OK) return st;
+    st = check_common(ndim, n_rec, Dv, Do, n_rot, n_pose, shift, n_sh);
+    if (st != TP_OK) return st;
+    const long long n_items = (long long)n_rec * n_pose;
+    const bool want_grad = grad_rot || (grad_shift && shift);
+    if (n_items > 0 && (grad_rec || want_grad)) {
+        if (!grad_out || !rot || (want_grad && !rec)) return TP_ERR_NULL;
+        if (!aligned(grad_out, 8) || !aligned(rot, 4) || (rec && !aligned(rec, 8)) ||
+            (shift && !aligned(shift, 4)))
+            return TP_ERR_VALUE;
+    }
+    if ((grad_rec && !aligned(grad_rec, 8)) || (grad_rot && !aligned(grad_rot, 4)) ||
+        (grad_shift && !aligned(grad_shift, 4)))
+        return TP_ERR_VALUE;
+    const tp::Geom g = make_geom(ndim, n_rec, Dv, n_rot, n_pose, shift, n_sh, Do, o);
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    const int k2 = ndim * ndim;
+    const size_t n_sh_rows = shift ? (size_t)n_sh : 1;
+    if (grad_rec && n_rec > 0 &&
+        cudaMemsetAsync(grad_rec, 0, (size_t)g.rec_elems * n_rec * 8, s) != cudaSuccess)
+        return TP_ERR_CUDA;
+    if (grad_rot && cudaMemsetAsync(grad_rot, 0, (size_t)n_rot * n_pose * k2 * 4, s) != cudaSuccess)
+        return TP_ERR_CUDA;
+    if (grad_shift && cudaMemsetAsync(grad_shift, 0, n_sh_rows * n_pose * 2 * 4, s) != cudaSuccess)
+        return TP_ERR_CUDA;
+    if (n_items == 0 || (!grad_rec && !want_grad)) return TP_OK;
+    const cudaError_t e = tp::launch_backward(ndim, o.interp, g, rec, rot, shift, grad_out,
+                                              grad_rec, grad_rot, grad_shift, sm_count(), s);
+    return e == cudaSuccess ? TP_OK : TP_ERR_CUDA;
+}
+
+const char* tp_status_string(tp_status status)
+{
+    switch (status) {
+    case TP_OK: return "TP_OK";
+    case TP_ERR_NULL: return "TP_ERR_NULL: a required pointer is NULL";
+    case TP_ERR_SHAPE: return "TP_ERR_SHAPE: a size is negative, odd, too large or mismatched";
+    case TP_ERR_VALUE: return "TP_ERR_VALUE: an option or flag is out of range, or a pointer is misaligned";
+    case TP_ERR_CUDA: return "TP_ERR_CUDA: a CUDA launch or memset failed";
+    }
+    return "TP_ERR_UNKNOWN: not a tp_status value";
+}
+
+}  // extern "C"

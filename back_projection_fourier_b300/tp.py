@@ -1,0 +1,220 @@
+"""Thin Python binding of libtp.so (include/tp.h), argument marshalling only.
+
+Every ``tp_*`` function here has the name of the C entry point it calls, takes torch
+tensors on the current CUDA device (complex64 spectra, float32 rotations / shifts /
+weights, C-contiguous) and derives the sizes from their shapes.  All the arithmetic runs
+in the CUDA kernels of libtp.so; there is no CPU or PyTorch fallback: importing this
+module fails when the library has not been built.
+
+The functional helpers at the end (``project``, ``backproject``, ``project_backward``)
+allocate the outputs with torch and call the ``tp_*`` functions.
+"""
+from __future__ import annotations
+
+import ctypes
+import re
+from pathlib import Path
+
+import torch
+
+PKG = Path(__file__).resolve().parent
+LIB_PATH = PKG / "libtp.so"
+HEADER = PKG.parent / "include" / "tp.h"
+
+TP_LINEAR, TP_CUBIC = 0, 1
+TP_LAYOUT_FFTW, TP_LAYOUT_CENTERED = 0, 1
+STATUS = {0: "TP_OK", 1: "TP_ERR_NULL", 2: "TP_ERR_SHAPE", 3: "TP_ERR_VALUE", 4: "TP_ERR_CUDA"}
+
+
+class tp_opts(ctypes.Structure):
+    _fields_ = [("interp", ctypes.c_int), ("layout", ctypes.c_int),
+                ("oversampling", ctypes.c_float), ("cutoff", ctypes.c_float)]
+
+
+class TPError(RuntimeError):
+    def __init__(self, status: int, what: str):
+        self.status = status
+        super().__init__(f"{what}: {lib().tp_status_string(status).decode()}")
+
+
+def _load() -> ctypes.CDLL:
+    if not LIB_PATH.exists():
+        raise ImportError(
+            f"{LIB_PATH} is missing: build it with `python -m back_projection_fourier_b300.build` "
+            "(there is no fallback implementation)")
+    L = ctypes.CDLL(str(LIB_PATH))
+    P, I = ctypes.c_void_p, ctypes.c_int
+    O = ctypes.POINTER(tp_opts)
+    L.tp_project_3d_to_2d.argtypes = [P, I, I, P, I, I, P, I, P, I, O, P]
+    L.tp_project_2d_to_2d.argtypes = [P, I, I, P, I, I, P, I, P, I, O, P]
+    L.tp_backproject_2d_to_3d.argtypes = [P, P, I, I, P, I, I, P, I, P, P, I, I, O, P]
+    L.tp_backproject_2d_to_2d.argtypes = [P, P, I, I, P, I, I, P, I, P, P, I, I, O, P]
+    L.tp_project_backward.argtypes = [I, P, I, I, P, I, I, P, I, P, I, P, P, P, O, P]
+    L.tp_status_string.argtypes = [I]
+    L.tp_status_string.restype = ctypes.c_char_p
+    for f in (L.tp_project_3d_to_2d, L.tp_project_2d_to_2d, L.tp_backproject_2d_to_3d,
+              L.tp_backproject_2d_to_2d, L.tp_project_backward):
+        f.restype = I
+    return L
+
+
+_LIB = _load()
+
+
+def lib() -> ctypes.CDLL:
+    return _LIB
+
+
+def header_symbols() -> list[str]:
+    """Names of the functions include/tp.h declares."""
+    text = HEADER.read_text()
+    return sorted(set(re.findall(r"^\s*(?:tp_status|const char\*)\s+(tp_\w+)\s*\(", text, re.M)))
+
+
+# ------------------------------------------------------------- marshalling ----
+
+def make_opts(interp=TP_CUBIC, layout=TP_LAYOUT_CENTERED, oversampling=1.0, cutoff=-1.0):
+    return tp_opts(int(interp), int(layout), float(oversampling), float(cutoff))
+
+
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream):
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return ctypes.c_void_p(stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream))
+
+
+def _need(t, dtype, name, ndim=None):
+    if t is None:
+        return
+    if t.dtype != dtype:
+        raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
+    if not t.is_cuda:
+        raise TypeError(f"{name} must be a CUDA tensor")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    if ndim is not None and t.dim() != ndim:
+        raise ValueError(f"{name} must have {ndim} dimensions, got {tuple(t.shape)}")
+
+
+def _rs(rot, shift, k):
+    _need(rot, torch.float32, "rot", 4)
+    if tuple(rot.shape[2:]) != (k, k):
+        raise ValueError(f"rot must be [n_rot][n_pose][{k}][{k}]")
+    _need(shift, torch.float32, "shift", 3)
+    n_sh = 1 if shift is None else shift.shape[0]
+    return rot.shape[0], rot.shape[1], n_sh
+
+
+def _call(status: int, what: str):
+    if status != 0:
+        raise TPError(status, what)
+
+
+def _opts(opts):
+    return ctypes.byref(opts if opts is not None else make_opts())
+
+
+# ------------------------------------------------------- C entry points ----
+
+def tp_project_3d_to_2d(vol, rot, shift, out, opts=None, stream=None):
+    _need(vol, torch.complex64, "vol", 4)
+    _need(out, torch.complex64, "out", 4)
+    n_rot, n_pose, n_sh = _rs(rot, shift, 3)
+    _call(_LIB.tp_project_3d_to_2d(_ptr(vol), vol.shape[0], vol.shape[1], _ptr(rot), n_rot, n_pose,
+                                   _ptr(shift), n_sh, _ptr(out), out.shape[2], _opts(opts),
+                                   _stream(stream)), "tp_project_3d_to_2d")
+
+
+def tp_project_2d_to_2d(img, rot, shift, out, opts=None, stream=None):
+    _need(img, torch.complex64, "img", 3)
+    _need(out, torch.complex64, "out", 4)
+    n_rot, n_pose, n_sh = _rs(rot, shift, 2)
+    _call(_LIB.tp_project_2d_to_2d(_ptr(img), img.shape[0], img.shape[1], _ptr(rot), n_rot, n_pose,
+                                   _ptr(shift), n_sh, _ptr(out), out.shape[2], _opts(opts),
+                                   _stream(stream)), "tp_project_2d_to_2d")
+
+
+def tp_backproject_2d_to_3d(proj, weights, rot, shift, vol_out, wvol_out, Dv, accumulate=False,
+                            opts=None, stream=None):
+    _need(proj, torch.complex64, "proj", 4)
+    _need(weights, torch.float32, "weights", 4)
+    _need(vol_out, torch.complex64, "vol_out", 4)
+    _need(wvol_out, torch.float32, "wvol_out", 4)
+    n_rot, n_pose, n_sh = _rs(rot, shift, 3)
+    _call(_LIB.tp_backproject_2d_to_3d(_ptr(proj), _ptr(weights), proj.shape[0], proj.shape[2],
+                                       _ptr(rot), n_rot, n_pose, _ptr(shift), n_sh, _ptr(vol_out),
+                                       _ptr(wvol_out), int(Dv), int(bool(accumulate)), _opts(opts),
+                                       _stream(stream)), "tp_backproject_2d_to_3d")
+
+
+def tp_backproject_2d_to_2d(proj, weights, rot, shift, img_out, wimg_out, Dv, accumulate=False,
+                            opts=None, stream=None):
+    _need(proj, torch.complex64, "proj", 4)
+    _need(weights, torch.float32, "weights", 4)
+    _need(img_out, torch.complex64, "img_out", 3)
+    _need(wimg_out, torch.float32, "wimg_out", 3)
+    n_rot, n_pose, n_sh = _rs(rot, shift, 2)
+    _call(_LIB.tp_backproject_2d_to_2d(_ptr(proj), _ptr(weights), proj.shape[0], proj.shape[2],
+                                       _ptr(rot), n_rot, n_pose, _ptr(shift), n_sh, _ptr(img_out),
+                                       _ptr(wimg_out), int(Dv), int(bool(accumulate)), _opts(opts),
+                                       _stream(stream)), "tp_backproject_2d_to_2d")
+
+
+def tp_project_backward(ndim, rec, rot, shift, grad_out, grad_rec, grad_rot, grad_shift,
+                        opts=None, stream=None):
+    _need(rec, torch.complex64, "rec", ndim + 1)
+    _need(grad_out, torch.complex64, "grad_out", 4)
+    _need(grad_rec, torch.complex64, "grad_rec", ndim + 1)
+    _need(grad_rot, torch.float32, "grad_rot", 4)
+    _need(grad_shift, torch.float32, "grad_shift", 3)
+    n_rot, n_pose, n_sh = _rs(rot, shift, ndim)
+    _call(_LIB.tp_project_backward(int(ndim), _ptr(rec), rec.shape[0], rec.shape[1], _ptr(rot), n_rot,
+                                   n_pose, _ptr(shift), n_sh, _ptr(grad_out), grad_out.shape[2],
+                                   _ptr(grad_rec), _ptr(grad_rot), _ptr(grad_shift), _opts(opts),
+                                   _stream(stream)), "tp_project_backward")
+
+
+def tp_status_string(status: int) -> str:
+    return _LIB.tp_status_string(int(status)).decode()
+
+
+# -------------------------------------------------------- functional API ----
+
+def project(rec, rot, shift=None, Do=None, opts=None, stream=None):
+    """Forward projection (3D->2D when rec is [n_rec][D][D][H], 2D->2D when [n_rec][D][H])."""
+    ndim = rec.dim() - 1
+    Do = rec.shape[1] if Do is None else int(Do)
+    out = torch.empty((rec.shape[0], rot.shape[1], Do, Do // 2 + 1), dtype=torch.complex64,
+                      device=rec.device)
+    (tp_project_3d_to_2d if ndim == 3 else tp_project_2d_to_2d)(rec, rot, shift, out, opts, stream)
+    return out
+
+
+def backproject(proj, rot, shift=None, weights=None, Dv=None, want_weights=True, opts=None,
+                stream=None, ndim=3):
+    """Back-projection (insertion) into fresh zeroed outputs: (rec, weight rec or None)."""
+    Dv = proj.shape[2] if Dv is None else int(Dv)
+    H = Dv // 2 + 1
+    shape = (proj.shape[0], Dv, Dv, H) if ndim == 3 else (proj.shape[0], Dv, H)
+    rec = torch.empty(shape, dtype=torch.complex64, device=proj.device)
+    wrec = torch.empty(shape, dtype=torch.float32, device=proj.device) if want_weights else None
+    fn = tp_backproject_2d_to_3d if ndim == 3 else tp_backproject_2d_to_2d
+    fn(proj, weights, rot, shift, rec, wrec, Dv, False, opts, stream)
+    return rec, wrec
+
+
+def project_backward(rec, rot, grad_out, shift=None, want_rec=True, want_rot=True,
+                     want_shift=True, opts=None, stream=None):
+    """Fused backward: (grad_rec, grad_rot, grad_shift), each None when not wanted."""
+    ndim = rec.dim() - 1
+    g_rec = torch.empty_like(rec) if want_rec else None
+    g_rot = torch.empty_like(rot) if want_rot else None
+    n_sh = shift.shape[0] if shift is not None else 1
+    g_sh = torch.empty((n_sh, rot.shape[1], 2), dtype=torch.float32, device=rec.device) \
+        if want_shift else None
+    tp_project_backward(ndim, rec, rot, shift, grad_out, g_rec, g_rot, g_sh, opts, stream)
+    return g_rec, g_rot, g_sh

@@ -1,0 +1,396 @@
+#!/usr/bin/env python3
+"""Benchmark: differentiable Fourier-slice projection, forward + fused backward.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+                    [--workload NAME] [--no-e2e] [--no-cpu-baseline]
+
+A step is one pass of the hot path over one batch: the forward projection of B poses
+(tp_project_3d_to_2d) and the fused backward for an upstream gradient
+(tp_project_backward: volume, rotation and shift gradients).  The default workload is
+D = 128 volume (128 x 128 x 65 complex64), B = 16384 uniform-SO(3) poses, shifts U(-5, 5)
+px, Catmull-Rom cubic, cutoff 64, centered layout.  Inputs are seeded and synthetic.
+
+Under torchrun (N > 1) every rank runs its own batch on its own GPU (weak scaling); the
+volume gradient is summed over ranks with one NCCL all-reduce per step.  Rank 0 prints one
+JSON line.  ``--impl reference`` times the fp64 CPU oracle on the host cores instead, on a
+bounded sample of the same workload (rank 0 only).
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+from pathlib import Path
+
+import numpy as np
+
+ROOT = Path(__file__).resolve().parent
+sys.path.insert(0, str(ROOT))
+
+METRIC = "projections/sec fwd+bwd at D=128 cubic; achieved GB/s vs HBM/L2 roofline"
+DEFAULT_WORKLOAD = "fwdbwd3d_d128_cubic_b16384"
+TRAFFIC_FILE = ROOT / "profiles" / "traffic.json"
+KERNEL_SOURCES = ["back_projection_fourier_b300/csrc/kernels.cu",
+                  "back_projection_fourier_b300/csrc/tp_device.cuh"]
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=10)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default=DEFAULT_WORKLOAD)
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-sample", type=int, default=1024, help="poses in the oracle sample")
+    return ap.parse_args()
+
+
+def dist_env():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+def cores() -> int:
+    try:
+        return len(os.sched_getaffinity(0))
+    except AttributeError:
+        return os.cpu_count() or 1
+
+
+def kernel_hash() -> str:
+    h = hashlib.sha256()
+    for rel in KERNEL_SOURCES:
+        h.update((ROOT / rel).read_bytes())
+    return h.hexdigest()[:16]
+
+
+# ----------------------------------------------------------------- oracle ----
+
+def oracle_fwdbwd_rate(wl, n_poses: int, nthreads: int) -> tuple[float, str]:
+    """Poses/s of the fp64 oracle's forward + backward on the first n_poses poses."""
+    import oracle
+
+    n = min(n_poses, wl.n_pose)
+    idx = np.arange(n)
+    take = lambda a: None if a is None else np.ascontiguousarray(a[:, idx])  # noqa: E731
+    kw = dict(interp=wl.interp, layout=wl.layout, cutoff=wl.rc, nthreads=nthreads)
+    rot, sh, g = take(wl.rot), take(wl.shift), take(wl.grad)
+    t0 = time.perf_counter()
+    oracle.project(wl.ndim, wl.rec, rot, sh, **kw)
+    oracle.project_backward(wl.ndim, wl.rec, rot, g, sh, **kw)
+    dt = time.perf_counter() - t0
+    return n / dt, f"first {n} of {wl.n_pose} poses, forward + full backward, fp64, {dt:.1f} s"
+
+
+def run_reference(args, wl):
+    world, rank, _ = dist_env()
+    if rank != 0:
+        return 0
+    nthreads = cores()
+    per_step = max(8, min(args.cpu_sample // 4, wl.n_pose))
+    import oracle
+
+    oracle.build()
+    for _ in range(args.warmup):
+        oracle_fwdbwd_rate(wl, per_step, nthreads)
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        oracle_fwdbwd_rate(wl, per_step, nthreads)
+    dt = time.perf_counter() - t0
+    value = per_step * args.steps / dt
+    sample = f"{per_step} of {wl.n_pose} poses per step (forward + full backward, fp64)"
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "projections/s",
+        "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": 1e3 * dt / args.steps * (wl.n_pose / per_step),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic", "config": workload_config(wl, "n/a (host oracle)"),
+        "cpu_baseline": {"value": value, "unit": "projections/s", "cores": nthreads,
+                         "kind": "oracle", "sample": sample},
+        "e2e": {"value": value, "unit": "projections/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+# ----------------------------------------------------------------- clocks ----
+
+class ClockSampler:
+    """nvidia-smi samples of SM clock and throttle reasons during the timed region."""
+
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, uuid: str | None):
+        self.proc = None
+        self.path = None
+        try:
+            fd, self.path = tempfile.mkstemp(suffix=".csv")
+            os.close(fd)
+            cmd = ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                   "-lms", "200"]
+            if uuid:
+                cmd += ["-i", uuid]
+            self.out = open(self.path, "w")
+            self.proc = subprocess.Popen(cmd, stdout=self.out, stderr=subprocess.DEVNULL)
+        except OSError:
+            self.proc = None
+
+    def stop(self) -> dict | None:
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.out.close()
+        rows = []
+        for line in Path(self.path).read_text().splitlines():
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 8:
+                continue
+            try:
+                rows.append((float(parts[0]), float(parts[1]), parts[4:8]))
+            except ValueError:
+                continue
+        os.unlink(self.path)
+        if not rows:
+            return None
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[k] for _, _, r in rows for k in range(4) if r[k].lower() == "active"})
+        sm = [r[0] for r in rows]
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(r[1] for r in rows),
+                "reasons": reasons, "samples": len(rows)}
+
+
+# ------------------------------------------------------------------ ours ----
+
+def workload_config(wl, l2: str) -> dict:
+    return {"workload": wl.name, "D": wl.D, "batch": wl.B, "interp": "cubic" if wl.interp else "linear",
+            "cutoff": wl.rc, "shift_amp": wl.extra["shift_amp"],
+            "layout": "centered" if wl.layout else "fftw", "step": "forward + fused backward",
+            "l2": l2}
+
+
+def hbm_bytes(wl):
+    """Algorithmic HBM bytes per launch: each unique input read once, each output written
+    once.  Per projection: Do*(Do/2+1)*8 B of image (written by the forward, read by the
+    backward) plus 4*(k*k+2) B of pose; per launch: the volume (and its gradient)."""
+    img = wl.D * wl.H * 8
+    k = wl.ndim
+    pose = 4 * (k * k + 2)
+    vol = wl.rec.nbytes
+    fwd = wl.B * (img + pose) + vol
+    bwd = wl.B * (img + 2 * pose) + 2 * vol
+    return fwd, bwd
+
+
+def kept_pixels(wl) -> int:
+    ky = np.arange(wl.D) - wl.D // 2
+    kx = np.arange(wl.H)
+    return int(((kx[None, :] ** 2 + ky[:, None] ** 2) <= wl.rc ** 2).sum())
+
+
+def run_ours(args, wl):
+    import torch
+    import torch.distributed as dist
+
+    world, rank, local = dist_env()
+    torch.cuda.set_device(local)
+    if world > 1:
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    from back_projection_fourier_b300 import tp
+
+    dev = torch.device("cuda", local)
+    stream = torch.cuda.current_stream(dev)
+    op = tp.make_opts(wl.interp, wl.layout, 1.0, wl.rc)
+    V = torch.from_numpy(wl.rec).to(dev)
+    R = torch.from_numpy(wl.rot).to(dev)
+    S = torch.from_numpy(wl.shift).to(dev) if wl.shift is not None else None
+    G = torch.from_numpy(wl.grad).to(dev)
+    Y = torch.empty_like(G)
+    gV = torch.empty_like(V)
+    gR = torch.empty_like(R)
+    gS = torch.empty((1 if S is None else S.shape[0], wl.n_pose, 2), device=dev)
+
+    def step(ev=None):
+        if ev is not None:
+            ev[0].record(stream)
+        tp.tp_project_3d_to_2d(V, R, S, Y, op, stream)
+        if ev is not None:
+            ev[1].record(stream)
+        tp.tp_project_backward(3, V, R, S, G, gV, gR, gS, op, stream)
+        if ev is not None:
+            ev[2].record(stream)
+        if world > 1:
+            dist.all_reduce(torch.view_as_real(gV))
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(args.steps)]
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    uuid = None
+    try:
+        uuid = str(torch.cuda.get_device_properties(dev).uuid)
+        uuid = uuid if uuid.startswith("GPU-") else "GPU-" + uuid
+    except Exception:
+        uuid = None
+    sampler = ClockSampler(uuid) if rank == 0 else None
+    time.sleep(0.3 if sampler else 0)
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    start.record(stream)
+    for k in range(args.steps):
+        step(evs[k])
+    end.record(stream)
+    torch.cuda.synchronize()
+    if world > 1:
+        dist.barrier()
+    clocks = sampler.stop() if sampler else None
+    ms = start.elapsed_time(end)
+    if world > 1:
+        t = torch.tensor([ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms = float(t.item())
+    fwd_ms = statistics.mean(e[0].elapsed_time(e[1]) for e in evs)
+    bwd_ms = statistics.mean(e[1].elapsed_time(e[2]) for e in evs)
+    ms_step = ms / args.steps
+    value = wl.B * world / (ms_step * 1e-3)
+
+    # e2e: host (pinned) inputs -> device -> forward + backward -> host outputs, every step
+    e2e = None
+    if not args.no_e2e:
+        hV, hR, hG = V.cpu().pin_memory(), R.cpu().pin_memory(), G.cpu().pin_memory()
+        hS = S.cpu().pin_memory() if S is not None else None
+        oY = torch.empty(Y.shape, dtype=Y.dtype, pin_memory=True)
+        ogV = torch.empty(gV.shape, dtype=gV.dtype, pin_memory=True)
+        ogR = torch.empty(gR.shape, dtype=gR.dtype, pin_memory=True)
+        ogS = torch.empty(gS.shape, dtype=gS.dtype, pin_memory=True)
+        dV, dR, dG = torch.empty_like(V), torch.empty_like(R), torch.empty_like(G)
+        dS = torch.empty_like(S) if S is not None else None
+
+        def e2e_step():
+            dV.copy_(hV, non_blocking=True)
+            dR.copy_(hR, non_blocking=True)
+            if dS is not None:
+                dS.copy_(hS, non_blocking=True)
+            dG.copy_(hG, non_blocking=True)
+            tp.tp_project_3d_to_2d(dV, dR, dS, Y, op, stream)
+            tp.tp_project_backward(3, dV, dR, dS, dG, gV, gR, gS, op, stream)
+            if world > 1:
+                dist.all_reduce(torch.view_as_real(gV))
+            oY.copy_(Y, non_blocking=True)
+            ogV.copy_(gV, non_blocking=True)
+            ogR.copy_(gR, non_blocking=True)
+            ogS.copy_(gS, non_blocking=True)
+
+        for _ in range(max(1, args.warmup)):
+            e2e_step()
+        torch.cuda.synchronize()
+        if world > 1:
+            dist.barrier()
+        t0 = time.perf_counter()
+        for _ in range(args.steps):
+            e2e_step()
+        torch.cuda.synchronize()
+        dt = time.perf_counter() - t0
+        if world > 1:
+            t = torch.tensor([dt], device=dev)
+            dist.all_reduce(t, op=dist.ReduceOp.MAX)
+            dt = float(t.item())
+        h2d = sum(x.numel() * x.element_size() for x in (hV, hR, hG) + ((hS,) if hS is not None else ()))
+        d2h = sum(x.numel() * x.element_size() for x in (oY, ogV, ogR, ogS))
+        e2e = {"value": wl.B * world / (dt / args.steps), "unit": "projections/s",
+               "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h}
+
+    # roofline of the dominant kernel
+    fwd_b, bwd_b = hbm_bytes(wl)
+    dom = "backward" if bwd_ms >= fwd_ms else "forward"
+    dom_ms, dom_b = (bwd_ms, bwd_b) if dom == "backward" else (fwd_ms, fwd_b)
+    peaks = {}
+    try:
+        peaks = json.loads((ROOT / "MEASURED_PEAKS.json").read_text())
+    except (OSError, ValueError):
+        pass
+    peak = peaks.get("hbm_gbs")
+    peak_src = "measured"
+    if peak is None:
+        peak, peak_src = 6400.0, "fallback"
+    achieved = dom_b / (dom_ms * 1e-3) / 1e9
+    traffic = None
+    try:
+        tr = json.loads(TRAFFIC_FILE.read_text())
+        ent = tr.get(wl.name, {}).get(dom)
+        if ent and ent.get("kernel_hash") == kernel_hash():
+            traffic = ent["dram_bytes_per_launch"]
+    except (OSError, ValueError):
+        pass
+    taps = kept_pixels(wl) * wl.B * (64 if wl.interp else 8)
+    l1_bytes = {"forward": taps * 8, "backward": taps * 8 * 2}[dom]
+    sm_mhz = (clocks or {}).get("sm_mhz") or peaks.get("sm_max_mhz", 2032.0)
+    l1_peak = 148 * 128 * sm_mhz * 1e6 / 1e9
+    roofline = {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
+                "frac": achieved / peak, "traffic": traffic, "kernel": dom,
+                "peak_source": peak_src, "kernel_ms": dom_ms}
+    onchip = {"bound": "l1", "achieved": l1_bytes / (dom_ms * 1e-3) / 1e9,
+              "peak": l1_peak, "unit": "GB/s", "frac": l1_bytes / (dom_ms * 1e-3) / 1e9 / l1_peak,
+              "kernel": dom, "peak_source": "derived: 148 SM x 128 B/clk x median SM clock",
+              "bytes": "taps x 8 B (forward gather) / taps x 16 B (backward gather + scatter)"}
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        rate, sample = oracle_fwdbwd_rate(wl, args.cpu_sample, cores())
+        cpu = {"value": rate, "unit": "projections/s", "cores": cores(), "kind": "oracle",
+               "sample": sample}
+
+    if rank == 0:
+        line = {
+            "metric": METRIC, "value": value, "unit": "projections/s", "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_step,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
+            "data": "synthetic (seeded rfft of N(0,1) volume, uniform SO(3), CN(0,1) upstream grad)",
+            "config": workload_config(wl, "inputs larger than L2 (1.09 GB upstream grad read and "
+                                          "1.09 GB projections written per step); no flush"),
+            "gpu_launches": 2 * args.steps,
+            "kernel_ms": {"forward": fwd_ms, "backward": bwd_ms},
+            "roofline": roofline, "roofline_onchip": onchip,
+            "cpu_baseline": cpu, "e2e": e2e, "clocks": clocks,
+        }
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        dist.destroy_process_group()
+    return 0
+
+
+def main():
+    args = parse()
+    from back_projection_fourier_b300 import synth
+
+    if args.impl == "reference":
+        world, rank, _ = dist_env()
+        if rank != 0:
+            return 0
+        return run_reference(args, synth.make_workload(args.workload))
+    wl = synth.make_workload(args.workload)
+    if wl.op != "fwdbwd" or wl.ndim != 3:
+        raise SystemExit("bench.py times the 3D forward + backward workloads")
+    return run_ours(args, wl)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -1,0 +1,146 @@
+/*
+ * tp.h -- C ABI of libtp.so: differentiable Fourier-slice projection on one NVIDIA B300
+ * (sm_103a).
+ *
+ * The operations are those of the torch-projectors paper summaries (gist.science):
+ *   - Method section, operations list: 3D->2D forward projection (central slice theorem),
+ *     2D->3D backward projection (accumulation into a 3D volume), 2D->2D forward (rotation
+ *     of 2D Fourier data) and 2D->2D backward (accumulation into a 2D reconstruction);
+ *     every operation supports rotation, translation by phase modulation and weight
+ *     accumulation ("useful for CTF correction");
+ *   - Method section, RFFT bullet: data are PyTorch/FFTW rfft half spectra;
+ *   - Method section, interpolation bullet: linear (bilinear / trilinear) or cubic
+ *     Catmull-Rom (Keys kernel, a = -0.5);
+ *   - Method section, Friedel bullet: F(-k) = conj F(k) of real functions, handled without
+ *     double counting on the zero-frequency axis;
+ *   - Method section, differentiation bullet: gradients for the inputs, the rotation
+ *     matrices and the shifts, computed without stored intermediates;
+ *   - Dutch page, Method section: shifts are applied by Fourier phase modulation.
+ *
+ * Definition (the pages give no formulas; this is the plainest reading they support):
+ *   Output pixel (i, j) of an image of box Do has kx = j in [0, Do/2] and ky = the frequency
+ *   of row i.  It is kept iff kx^2 + ky^2 <= rc^2, else it is 0.  A kept pixel samples the
+ *   reconstruction at c = o * R * q, q = (kx, ky, 0) (3D) or (kx, ky) (2D), R row-major
+ *   with vector order (x, y, z) <-> tensor axes (last, middle, first):
+ *       v(c) = sum_t w(c - t) V_ext(t)        (separable weights, taps floor(c)+{0,1} for
+ *                                              linear, floor(c)+{-1,0,1,2} for cubic)
+ *       V_ext(t) = V[t] if t_x >= 0, conj(V[-t]) if t_x < 0, and 0 where the stored
+ *                  frequency lies outside x in [0, Dv/2], y, z in [-Dv/2, Dv/2 - 1]
+ *       y = v(c) * exp(-2 pi i (kx sx + ky sy) / Do)
+ *   Back-projection is the exact real-linear transpose of this map under
+ *   <a, b> = Re sum conj(a) b; the weight accumulation scatters a real per-pixel weight
+ *   with the same interpolation weights (no phase, no conjugation).
+ *
+ * Layout (all arrays C-contiguous; complex = interleaved (re, im) fp32, 8-byte aligned):
+ *   3D reconstruction  [n_rec][Dv][Dv][Dv/2+1]   axes (z, y, x); x is the half axis
+ *   2D reconstruction  [n_rec][Dv][Dv/2+1]       axes (y, x)
+ *   images             [n_rec][n_pose][Do][Do/2+1]
+ *   rot                [n_rot][n_pose][k][k] fp32, k = 3 (3D) or 2 (2D), n_rot in {1, n_rec};
+ *                      n_rot = 1 shares one set of poses between all reconstructions
+ *   shift              [n_sh][n_pose][2] fp32 (sx, sy) in image pixels, n_sh in {1, n_rec};
+ *                      NULL means no shift
+ *   weights            fp32 with the image shape; NULL means weight 1
+ *   Full (non-half) axes are in FFTW order (index i holds i for i < D/2, else i - D) or
+ *   centered order (index i holds i - D/2), chosen by tp_opts.layout for every array.
+ *
+ * Ownership and execution: every pointer is a caller-owned DEVICE pointer on the current
+ * CUDA device.  The library allocates no device memory and keeps no state between calls.
+ * Work is enqueued on `stream` (a cudaStream_t; NULL = the legacy default stream) and
+ * the call returns without synchronising.  Outputs must not alias inputs.
+ *
+ * Errors: arguments are checked on the host before anything is enqueued; a rejected call
+ * enqueues nothing.  TP_ERR_CUDA reports a launch error (cudaGetLastError after the
+ * launches).  Errors of the asynchronous execution itself surface at the caller's next
+ * synchronisation.  No exception crosses the ABI and no kernel traps.
+ *
+ * Limits: Dv, Do even, 2 <= D; 3D boxes up to 1024, 2D boxes up to 32768; n_rec, n_pose,
+ * n_rot, n_sh >= 0; n_rec * n_pose images of Do*(Do/2+1) pixels each (64-bit offsets).
+ */
+#ifndef TP_H
+#define TP_H
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum tp_status {
+    TP_OK = 0,
+    TP_ERR_NULL = 1,  /* a required pointer is NULL */
+    TP_ERR_SHAPE = 2, /* a size is negative, odd, too large, or n_rot / n_sh mismatch */
+    TP_ERR_VALUE = 3, /* bad interp / layout, non-positive or non-finite oversampling,
+                         non-finite cutoff, ndim not 2 or 3, accumulate not 0 or 1 */
+    TP_ERR_CUDA = 4   /* a CUDA launch or memset failed */
+} tp_status;
+
+enum { TP_LINEAR = 0, TP_CUBIC = 1 };
+enum { TP_LAYOUT_FFTW = 0, TP_LAYOUT_CENTERED = 1 };
+
+/* Options shared by every call; a NULL tp_opts* means
+ * { TP_CUBIC, TP_LAYOUT_CENTERED, 1.0f, -1.0f }. */
+typedef struct tp_opts {
+    int interp;         /* TP_LINEAR or TP_CUBIC */
+    int layout;         /* TP_LAYOUT_FFTW or TP_LAYOUT_CENTERED */
+    float oversampling; /* o > 0: sample coordinate scale (Dv = o * Do for a padded volume) */
+    float cutoff;       /* rc in image frequency units; < 0 means Do / 2 */
+} tp_opts;
+
+/* 3D->2D forward projection (central slices).  Operations list, "3D -> 2D forward".
+ *   vol   [n_rec][Dv][Dv][Dv/2+1] complex (read)
+ *   out   [n_rec][n_pose][Do][Do/2+1] complex (overwritten; pixels beyond rc are 0) */
+tp_status tp_project_3d_to_2d(const void* vol, int n_rec, int Dv, const float* rot, int n_rot,
+                              int n_pose, const float* shift, int n_sh, void* out, int Do,
+                              const tp_opts* opts, void* stream);
+
+/* 2D->3D back-projection (insertion), the adjoint of tp_project_3d_to_2d, plus the weight
+ * accumulation.  Operations list, "2D -> 3D backward".
+ *   proj      [n_rec][n_pose][Do][Do/2+1] complex (read); data are multiplied by
+ *             conj(phase) and scattered with the transpose of the forward weights
+ *   weights   fp32 image-shaped per-pixel weights (read; NULL = 1)
+ *   vol_out   [n_rec][Dv][Dv][Dv/2+1] complex (NULL = skip the data)
+ *   wvol_out  [n_rec][Dv][Dv][Dv/2+1] fp32 (NULL = skip the weights)
+ *   accumulate 1 adds into the outputs; 0 zeroes them first */
+tp_status tp_backproject_2d_to_3d(const void* proj, const float* weights, int n_rec, int Do,
+                                  const float* rot, int n_rot, int n_pose, const float* shift,
+                                  int n_sh, void* vol_out, float* wvol_out, int Dv,
+                                  int accumulate, const tp_opts* opts, void* stream);
+
+/* 2D->2D forward (rotation of 2D Fourier data).  Operations list, "2D -> 2D forward".
+ *   img   [n_rec][Dv][Dv/2+1] complex (read); rot [n_rot][n_pose][2][2]
+ *   out   [n_rec][n_pose][Do][Do/2+1] complex (overwritten) */
+tp_status tp_project_2d_to_2d(const void* img, int n_rec, int Dv, const float* rot, int n_rot,
+                              int n_pose, const float* shift, int n_sh, void* out, int Do,
+                              const tp_opts* opts, void* stream);
+
+/* 2D->2D backward (accumulation into a 2D reconstruction), the adjoint of
+ * tp_project_2d_to_2d, plus the weight accumulation.  Operations list, "2D -> 2D backward".
+ *   img_out [n_rec][Dv][Dv/2+1] complex, wimg_out fp32 (each NULL = skip); other arguments
+ *   as in tp_backproject_2d_to_3d */
+tp_status tp_backproject_2d_to_2d(const void* proj, const float* weights, int n_rec, int Do,
+                                  const float* rot, int n_rot, int n_pose, const float* shift,
+                                  int n_sh, void* img_out, float* wimg_out, int Dv,
+                                  int accumulate, const tp_opts* opts, void* stream);
+
+/* Fused backward of tp_project_3d_to_2d (ndim = 3) or tp_project_2d_to_2d (ndim = 2) for
+ * the upstream gradient grad_out = dL/dRe(out) + i dL/dIm(out).  Differentiation bullet.
+ *   grad_rec   reconstruction-shaped complex: the transpose of the projection applied to
+ *              grad_out (overwritten; NULL = skip)
+ *   grad_rot   [n_rot][n_pose][k][k] fp32: dL/dR[a][b] = sum o q_b Re(conj(g') dv/dc_a),
+ *              g' = grad_out * conj(phase); summed over reconstructions when n_rot = 1;
+ *              the z column (3D) is 0 because q_z = 0 (overwritten; NULL = skip)
+ *   grad_shift [n_sh][n_pose][2] fp32: dL/ds = sum Re(conj(grad_out) y (-2 pi i k / Do)),
+ *              summed over reconstructions when n_sh = 1 (overwritten; NULL = skip).
+ *              When shift is NULL, n_sh is ignored and grad_shift, if given, is
+ *              [1][n_pose][2] and is set to 0 */
+tp_status tp_project_backward(int ndim, const void* rec, int n_rec, int Dv, const float* rot,
+                              int n_rot, int n_pose, const float* shift, int n_sh,
+                              const void* grad_out, int Do, void* grad_rec, float* grad_rot,
+                              float* grad_shift, const tp_opts* opts, void* stream);
+
+/* Static, NUL-terminated name of a status code (never NULL). */
+const char* tp_status_string(tp_status status);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* TP_H */

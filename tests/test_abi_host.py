@@ -1,0 +1,102 @@
+"""C-ABI checks that need no GPU: the library loads, exports every function the header
+declares, and rejects bad arguments on the host (before any CUDA call) with the status
+the header documents."""
+import ctypes
+import math
+import subprocess
+
+import pytest
+
+from back_projection_fourier_b300 import build as tp_build
+
+tp_build.build()
+from back_projection_fourier_b300 import tp  # noqa: E402
+
+L = tp.lib()
+FAKE = 0x10000          # aligned, never dereferenced: validation fails first
+MIS = 0x10004           # 4-byte aligned, not 8-byte aligned
+
+
+def test_header_symbols_are_exported():
+    names = tp.header_symbols()
+    assert set(names) == {"tp_project_3d_to_2d", "tp_backproject_2d_to_3d", "tp_project_2d_to_2d",
+                          "tp_backproject_2d_to_2d", "tp_project_backward", "tp_status_string"}
+    for n in names:
+        assert hasattr(L, n), n
+    dyn = subprocess.run(["nm", "-D", "--defined-only", str(tp.LIB_PATH)], capture_output=True,
+                         text=True, check=True).stdout
+    exported = {line.split()[-1] for line in dyn.splitlines() if " T " in line}
+    assert set(names) <= exported
+
+
+def test_status_strings():
+    for code, name in tp.STATUS.items():
+        assert tp.tp_status_string(code).startswith(name)
+    assert "UNKNOWN" in tp.tp_status_string(99)
+
+
+def opts(interp=1, layout=1, o=1.0, cutoff=-1.0):
+    return ctypes.byref(tp.make_opts(interp, layout, o, cutoff))
+
+
+def proj3(vol=FAKE, n_rec=1, Dv=8, rot=FAKE, n_rot=1, n_pose=2, shift=None, n_sh=1, out=FAKE,
+          Do=8, o=None):
+    return L.tp_project_3d_to_2d(vol, n_rec, Dv, rot, n_rot, n_pose, shift, n_sh, out, Do,
+                                 o if o is not None else opts(), None)
+
+
+def test_project_argument_errors():
+    assert proj3(vol=None) == 1
+    assert proj3(rot=None) == 1
+    assert proj3(out=None) == 1
+    assert proj3(Dv=7) == 2
+    assert proj3(Do=0) == 2
+    assert proj3(Dv=2048) == 2
+    assert proj3(n_rec=-1) == 2
+    assert proj3(n_pose=-3) == 2
+    assert proj3(n_rec=3, n_rot=2) == 2
+    assert proj3(n_rec=3, n_rot=3, shift=FAKE, n_sh=2) == 2
+    assert proj3(o=opts(interp=2)) == 3
+    assert proj3(o=opts(layout=-1)) == 3
+    assert proj3(o=opts(o=0.0)) == 3
+    assert proj3(o=opts(o=-1.0)) == 3
+    assert proj3(o=opts(o=math.inf)) == 3
+    assert proj3(o=opts(cutoff=math.nan)) == 3
+    assert proj3(vol=MIS) == 3
+    assert proj3(out=MIS) == 3
+    # empty batches are valid and enqueue nothing
+    assert proj3(n_rec=0, vol=None, rot=None, out=None) == 0
+    assert proj3(n_pose=0, vol=None, rot=None, out=None) == 0
+    assert L.tp_project_2d_to_2d(FAKE, 1, 40000, FAKE, 1, 1, None, 1, FAKE, 8, None, None) == 2
+
+
+def test_backproject_argument_errors():
+    bp = L.tp_backproject_2d_to_3d
+    assert bp(FAKE, None, 1, 8, FAKE, 1, 2, None, 1, FAKE, None, 8, 2, opts(), None) == 3
+    assert bp(None, None, 1, 8, FAKE, 1, 2, None, 1, FAKE, None, 8, 0, opts(), None) == 1
+    assert bp(FAKE, None, 1, 8, None, 1, 2, None, 1, FAKE, None, 8, 0, opts(), None) == 1
+    assert bp(FAKE, None, 1, 9, FAKE, 1, 2, None, 1, FAKE, None, 8, 0, opts(), None) == 2
+    assert bp(FAKE, None, 1, 8, FAKE, 1, 2, None, 1, MIS, None, 8, 0, opts(), None) == 3
+    assert bp(FAKE, None, 0, 8, FAKE, 1, 2, None, 1, FAKE, None, 8, 0, opts(), None) == 0
+    bp2 = L.tp_backproject_2d_to_2d
+    assert bp2(FAKE, None, 2, 8, FAKE, 3, 1, None, 1, FAKE, None, 8, 0, opts(), None) == 2
+
+
+def test_backward_argument_errors():
+    bw = L.tp_project_backward
+    assert bw(4, FAKE, 1, 8, FAKE, 1, 2, None, 1, FAKE, 8, FAKE, None, None, opts(), None) == 3
+    assert bw(3, FAKE, 1, 8, FAKE, 1, 2, None, 1, None, 8, FAKE, None, None, opts(), None) == 1
+    assert bw(3, None, 1, 8, FAKE, 1, 2, None, 1, FAKE, 8, None, FAKE, None, opts(), None) == 1
+    assert bw(3, FAKE, 1, 8, FAKE, 1, 2, None, 1, FAKE, 6, FAKE, None, None, opts(cutoff=math.inf), None) == 3
+    assert bw(2, FAKE, 2, 8, FAKE, 1, 2, FAKE, 3, FAKE, 8, FAKE, None, None, opts(), None) == 2
+
+
+def test_binding_rejects_bad_tensors():
+    import torch
+    vol = torch.zeros((1, 8, 8, 5), dtype=torch.complex64)
+    rot = torch.zeros((1, 2, 3, 3))
+    out = torch.zeros((1, 2, 8, 5), dtype=torch.complex64)
+    with pytest.raises(TypeError):
+        tp.tp_project_3d_to_2d(vol, rot, None, out)          # CPU tensors
+    with pytest.raises(TypeError):
+        tp.tp_project_3d_to_2d(vol.real.contiguous(), rot, None, out)

@@ -1,0 +1,163 @@
+"""GPU parity: every C-ABI entry point against the fp64 oracle on the same seeded inputs.
+
+Small cases span several CTAs and ragged pixel tails, both interpolations and layouts,
+2D and 3D, oversampling, custom cutoffs, shifts on/off, several reconstructions with
+shared or per-reconstruction poses.  Metric: max |gpu - oracle| / max |oracle| per output
+tensor; bar: 1e-5 for forward projection, 1e-4 for back-projection and gradients.
+"""
+import numpy as np
+import pytest
+import torch
+
+from parity_util import TOL_BWD, TOL_FWD, crandn32, dev, host, max_rel, opts, oracle, rotations
+from back_projection_fourier_b300 import tp
+
+pytestmark = pytest.mark.gpu
+
+# ndim, interp, layout, o, Dv, Do, cutoff, shifted, n_rec, n_rot, n_pose
+CASES = [
+    (3, 1, 1, 1.0, 32, 32, -1.0, True, 1, 1, 37),
+    (3, 0, 1, 1.0, 32, 32, -1.0, True, 1, 1, 37),
+    (3, 1, 0, 1.0, 24, 24, 9.5, True, 2, 2, 13),
+    (3, 0, 0, 1.5, 24, 16, -1.0, False, 2, 1, 11),
+    (3, 1, 1, 2.0, 32, 16, 100.0, True, 1, 1, 9),
+    (3, 1, 1, 1.0, 2, 2, -1.0, True, 1, 1, 5),
+    (2, 1, 1, 1.0, 48, 48, -1.0, True, 5, 5, 3),
+    (2, 0, 0, 1.0, 30, 30, -1.0, True, 3, 1, 4),
+    (2, 1, 0, 1.5, 36, 24, 10.0, False, 4, 4, 2),
+    (2, 0, 1, 1.0, 64, 64, 0.0, True, 2, 2, 3),
+]
+
+
+def make_case(case, seed=0):
+    ndim, interp, layout, o, Dv, Do, rc, shifted, n_rec, n_rot, n_pose = case
+    rng = np.random.default_rng(seed + hash(case) % 10000)
+    Hv, Ho = Dv // 2 + 1, Do // 2 + 1
+    shape = (n_rec, Dv, Dv, Hv) if ndim == 3 else (n_rec, Dv, Hv)
+    rec = crandn32(rng, shape)
+    rot = rotations(rng, n_rot * n_pose, ndim).reshape(n_rot, n_pose, ndim, ndim)
+    shift = rng.uniform(-6, 6, (n_rot, n_pose, 2)).astype(np.float32) if shifted else None
+    grad = crandn32(rng, (n_rec, n_pose, Do, Ho))
+    w = rng.uniform(0.0, 2.0, (n_rec, n_pose, Do, Ho)).astype(np.float32)
+    kw = dict(interp=interp, layout=layout, oversampling=o, cutoff=rc)
+    return rec, rot, shift, grad, w, kw, opts(interp, layout, o, rc)
+
+
+@pytest.mark.parametrize("case", CASES, ids=[str(c) for c in CASES])
+def test_forward(case):
+    ndim, Do = case[0], case[5]
+    rec, rot, shift, _, _, kw, op = make_case(case)
+    y = tp.project(dev(rec), dev(rot), dev(shift), Do=Do, opts=op)
+    ref = oracle.project(ndim, rec, rot, shift, Do=Do, **kw)
+    assert max_rel(host(y), ref) <= TOL_FWD
+
+
+@pytest.mark.parametrize("case", CASES, ids=[str(c) for c in CASES])
+def test_backward(case):
+    ndim = case[0]
+    rec, rot, shift, grad, _, kw, op = make_case(case, seed=1)
+    g_rec, g_rot, g_sh = tp.project_backward(dev(rec), dev(rot), dev(grad), dev(shift),
+                                             want_shift=shift is not None, opts=op)
+    r_rec, r_rot, r_sh = oracle.project_backward(ndim, rec, rot, grad, shift, **kw)
+    assert max_rel(host(g_rec), r_rec) <= TOL_BWD
+    assert max_rel(host(g_rot), r_rot) <= TOL_BWD
+    if ndim == 3:
+        assert np.all(host(g_rot)[..., 2] == 0)
+    if shift is not None:
+        assert max_rel(host(g_sh), r_sh) <= TOL_BWD
+
+
+@pytest.mark.parametrize("case", CASES[:3] + CASES[6:8], ids=[str(c) for c in CASES[:3] + CASES[6:8]])
+def test_backward_partial_outputs(case):
+    """Each gradient output may be skipped (NULL); the others are unchanged."""
+    ndim = case[0]
+    rec, rot, shift, grad, _, kw, op = make_case(case, seed=2)
+    r_rec, r_rot, r_sh = oracle.project_backward(ndim, rec, rot, grad, shift, **kw)
+    g_rec, _, _ = tp.project_backward(dev(rec), dev(rot), dev(grad), dev(shift), want_rot=False,
+                                      want_shift=False, opts=op)
+    assert max_rel(host(g_rec), r_rec) <= TOL_BWD
+    _, g_rot, g_sh = tp.project_backward(dev(rec), dev(rot), dev(grad), dev(shift), want_rec=False,
+                                         want_shift=shift is not None, opts=op)
+    assert max_rel(host(g_rot), r_rot) <= TOL_BWD
+    if shift is not None:
+        assert max_rel(host(g_sh), r_sh) <= TOL_BWD
+    # without a shift the shift gradient is defined as zero
+    _, _, g0 = tp.project_backward(dev(rec), dev(rot), dev(grad), None, want_rec=False, opts=op)
+    assert np.all(host(g0) == 0)
+
+
+@pytest.mark.parametrize("case", CASES, ids=[str(c) for c in CASES])
+@pytest.mark.parametrize("with_weights", [True, False])
+def test_backproject(case, with_weights):
+    ndim, Dv = case[0], case[4]
+    _, rot, shift, proj, w, kw, op = make_case(case, seed=3)
+    weights = w if with_weights else None
+    vol, wvol = tp.backproject(dev(proj), dev(rot), dev(shift), dev(weights), Dv=Dv, opts=op,
+                               ndim=ndim)
+    r_vol, r_w = oracle.backproject(ndim, proj, rot, weights=weights, shift=shift, Dv=Dv, **kw)
+    assert max_rel(host(vol), r_vol) <= TOL_BWD
+    assert max_rel(host(wvol), r_w) <= TOL_BWD
+
+
+@pytest.mark.parametrize("ndim", [2, 3])
+def test_backproject_accumulate_and_skips(ndim):
+    case = (ndim, 1, 1, 1.0, 24, 24, -1.0, True, 2, 2, 5)
+    _, rot, shift, proj, w, kw, op = make_case(case, seed=4)
+    r_vol, r_w = oracle.backproject(ndim, proj, rot, weights=w, shift=shift, Dv=24, **kw)
+    vol, wvol = tp.backproject(dev(proj), dev(rot), dev(shift), dev(w), Dv=24, opts=op, ndim=ndim)
+    fn = tp.tp_backproject_2d_to_3d if ndim == 3 else tp.tp_backproject_2d_to_2d
+    fn(dev(proj), dev(w), dev(rot), dev(shift), vol, wvol, 24, True, op)       # accumulate
+    assert max_rel(host(vol), 2 * r_vol) <= TOL_BWD
+    assert max_rel(host(wvol), 2 * r_w) <= TOL_BWD
+    # weights only (no data output), then data only, each overwriting (accumulate = 0)
+    fn(dev(proj), dev(w), dev(rot), dev(shift), None, wvol, 24, False, op)
+    assert max_rel(host(wvol), r_w) <= TOL_BWD
+    fn(dev(proj), None, dev(rot), dev(shift), vol, None, 24, False, op)
+    assert max_rel(host(vol), r_vol) <= TOL_BWD
+
+
+def test_empty_batches():
+    vol = torch.ones((1, 8, 8, 5), dtype=torch.complex64, device="cuda")
+    rot = torch.zeros((1, 0, 3, 3), device="cuda")
+    out = torch.empty((1, 0, 8, 5), dtype=torch.complex64, device="cuda")
+    tp.tp_project_3d_to_2d(vol, rot, None, out)
+    w = torch.ones((1, 8, 8, 5), device="cuda")
+    tp.tp_backproject_2d_to_3d(out, None, rot, None, vol, w, 8, False)   # zeroes the outputs
+    torch.cuda.synchronize()
+    assert torch.all(vol == 0) and torch.all(w == 0)
+    g_rot = torch.full((1, 0, 3, 3), 7.0, device="cuda")
+    tp.tp_project_backward(3, vol, rot, None, out, vol, g_rot, None)
+    torch.cuda.synchronize()
+
+
+def test_many_items_grid_stride():
+    """More work units than one grid holds: the kernels stride over items."""
+    rng = np.random.default_rng(7)
+    n_pose = 90000
+    rec = crandn32(rng, (1, 4, 4, 3))
+    rot = rotations(rng, n_pose, 3)[None]
+    shift = rng.uniform(-1, 1, (1, n_pose, 2)).astype(np.float32)
+    y = tp.project(dev(rec), dev(rot), dev(shift), opts=opts(1))
+    items = rng.integers(0, n_pose, 3000)
+    pix = rng.integers(0, 4 * 3, 3000)
+    ref = oracle.project_samples(3, rec, rot, items, pix, shift, interp=1)
+    got = host(y).reshape(n_pose, -1)[items, pix]
+    assert max_rel(got, ref) <= TOL_FWD
+    grec, grot, gsh = tp.project_backward(dev(rec), dev(rot), dev(crandn32(rng, (1, n_pose, 4, 3))),
+                                          dev(shift), opts=opts(1))
+    torch.cuda.synchronize()
+    assert torch.isfinite(grot).all()
+
+
+def test_large_box_sampled():
+    """D = 512 volume (32-bit in-volume offsets near their largest use) on a few poses."""
+    rng = np.random.default_rng(8)
+    D = 512
+    rec = crandn32(rng, (1, D, D, D // 2 + 1))
+    rot = rotations(rng, 3, 3)[None]
+    shift = rng.uniform(-20, 20, (1, 3, 2)).astype(np.float32)
+    y = host(tp.project(dev(rec), dev(rot), dev(shift), opts=opts(1)))
+    items = rng.integers(0, 3, 4000)
+    pix = rng.integers(0, D * (D // 2 + 1), 4000)
+    ref = oracle.project_samples(3, rec, rot, items, pix, shift, interp=1)
+    assert max_rel(y.reshape(3, -1)[items, pix], ref) <= TOL_FWD
