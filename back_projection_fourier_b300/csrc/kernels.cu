@@ -1,4 +1,4 @@
-// kernels.cu -- forward projection, fused backward and back-projection kernels.
+// kernels.cu -- forward projection, backward gradients and back-projection kernels.
 //
 // Operations (torch-projectors paper summaries, gist.science, Method section, list of
 // operations): 3D->2D forward (central slice theorem), 2D->3D backward (accumulation in a
@@ -6,19 +6,32 @@
 // (accumulation into a 2D reconstruction); gradients for inputs, rotations and shifts
 // without stored intermediates (differentiation bullet); shifts by phase modulation.
 //
-// Work decomposition: a CTA owns one item (reconstruction r, pose p) -- or 1/splits of
-// its pixels when items are too few to fill the GPU -- and stages the item's rotation and
-// shift once.  Threads stride over the item's pixels in row-major (ky, kx) order, so
-// image reads and writes are coalesced; the volume is read through the read-only path
-// and stays L2-resident (a D = 256 half volume is 68 MB of a 126 MB L2).
+// Gather kernels (forward projection; rotation / shift gradients).  A CTA owns one item
+// (reconstruction r, pose p) at a time (grid-stride over items) and stages the item's
+// rotation and shift.  Threads walk only the kept pixels (kx^2 + ky^2 <= rc^2) through a
+// per-CTA table of row offsets, in row-major order, so image reads and writes stay
+// coalesced.  Pixels whose taps are all read directly (the vast majority, see gather.cuh)
+// take the fast path; the others -- taps on the x = 0 plane or past x = Dv/2 -- are queued
+// in shared memory and evaluated densely with the exact per-tap rule, so they do not make
+// whole warps diverge.  The volume is read through the read-only path and stays
+// L2-resident (a D = 256 half volume is 68 MB of a 126 MB L2).
+#include "gather.cuh"
 #include "kernels.h"
-#include "tp_device.cuh"
+#include "scatter.cuh"
+
+// Width of the vector window used by the gather fast path: 1 (8-byte taps), 2 (16-byte
+// loads) or 4 (32-byte loads).
+#ifndef TP_GATHER_WIN
+#define TP_GATHER_WIN 2
+#endif
 
 namespace tp {
 
 namespace {
 
 constexpr int kThreads = 256;
+constexpr int kQueue = 2 * kThreads;
+constexpr int kMaxTableRows = 4096;  // image boxes up to this size use the kept-pixel table
 
 struct ItemRange {
     long long item;
@@ -35,10 +48,212 @@ __device__ __forceinline__ ItemRange item_of(const Geom& g, long long w, int spl
     return ir;
 }
 
+// ------------------------------------------------------------ shared tables ----
+
+__device__ __forceinline__ int isqrt_floor(int m)
+{
+    int k = (int)sqrtf((float)m);
+    while (k > 0 && k * k > m) --k;
+    while ((k + 1) * (k + 1) <= m) ++k;
+    return k;
+}
+
+// Kept pixels of image row i: kx in [0, count).
+__device__ __forceinline__ int row_kept(const Geom& g, int i)
+{
+    const int ky = row_freq(i, g.Do, g.halfo, g.centered);
+    const int m = g.rc2 - ky * ky;
+    if (m < 0) return 0;
+    const int k = isqrt_floor(m);
+    return (k < g.halfo ? k : g.halfo) + 1;
+}
+
+// rowstart[i] = kept pixels in rows < i, for i = 0..Do (exclusive block scan).
+__device__ void build_rowstart(const Geom& g, int* rowstart, int* scratch)
+{
+    const int per = (g.Do + kThreads - 1) / kThreads;
+    const int i0 = threadIdx.x * per;
+    int sum = 0;
+    for (int k = 0; k < per; ++k)
+        if (i0 + k < g.Do) sum += row_kept(g, i0 + k);
+    // inclusive warp scan, then the warp totals
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    int inc = sum;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const int v = __shfl_up_sync(0xffffffffu, inc, o);
+        if (lane >= o) inc += v;
+    }
+    if (lane == 31) scratch[warp] = inc;
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        int acc = 0;
+        for (int w = 0; w < kThreads / 32; ++w) {
+            const int t = scratch[w];
+            scratch[w] = acc;
+            acc += t;
+        }
+    }
+    __syncthreads();
+    int run = scratch[warp] + inc - sum;
+    for (int k = 0; k < per; ++k)
+        if (i0 + k < g.Do) {
+            rowstart[i0 + k] = run;
+            run += row_kept(g, i0 + k);
+        }
+    if (threadIdx.x == kThreads - 1) rowstart[g.Do] = run;
+    __syncthreads();
+}
+
+// Slow-path queue: pixels packed as (row << 16) | kx.
+struct Queue {
+    int* slots;  // [kQueue]
+    int* count;  // shared counter
+};
+
+__device__ __forceinline__ void enqueue(Queue q, bool slow, int row, int kx)
+{
+    const unsigned mask = __ballot_sync(0xffffffffu, slow);
+    if (!mask) return;
+    const int lane = threadIdx.x & 31;
+    int base = 0;
+    if (lane == __ffs(mask) - 1) base = atomicAdd(q.count, __popc(mask));
+    base = __shfl_sync(0xffffffffu, base, __ffs(mask) - 1);
+    if (slow) q.slots[base + __popc(mask & ((1u << lane) - 1))] = (row << 16) | kx;
+}
+
+// Sum of a per-thread value over the CTA, valid in thread 0.
+__device__ __forceinline__ float block_sum(float v, float* red)
+{
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    __syncthreads();
+    if (lane == 0) red[warp] = v;
+    __syncthreads();
+    float s = 0.f;
+    if (threadIdx.x == 0)
+        for (int k = 0; k < kThreads / 32; ++k) s += red[k];
+    return s;
+}
+
+// ------------------------------------------------------- per-pixel evaluation ----
+
+// Exact per-tap evaluation in the original frame (any pixel).
+template <int NDIM, int INTERP, bool DERIV>
+__device__ __forceinline__ void eval_general(const Geom& g, const float2* __restrict__ V,
+                                             const float* R, int kx, int ky, float2& v,
+                                             float2* dv)
+{
+    PixelTaps<NDIM, INTERP, DERIV> t;
+    t.init(g, R, (float)kx, (float)ky);
+    gather<NDIM, INTERP, DERIV>(V, g, t, v, dv);
+}
+
+// Effective-frame evaluation; false when the pixel needs the general path.
+template <int NDIM, int INTERP, int WIN, bool DERIV>
+__device__ __forceinline__ bool eval_fast(const Geom& g, const float2* __restrict__ V,
+                                          const float* R, int kx, int ky, float2& v, float2* dv)
+{
+    FastTaps<NDIM, INTERP, DERIV> t;
+    bool flip;
+    if (!fast_taps<NDIM, INTERP, DERIV>(g, R, (float)kx, (float)ky, t, flip)) return false;
+    gather_fast<NDIM, INTERP, WIN, DERIV>(V, t, v, dv);
+    if (flip) {
+        // v(c) = conj(v'(-c)); dv/dc = -conj(dv'/dc')
+        v.y = -v.y;
+        if constexpr (DERIV) {
+#pragma unroll
+            for (int a = 0; a < 3; ++a) dv[a].x = -dv[a].x;
+        }
+    }
+    return true;
+}
+
 // ------------------------------------------------------------------ forward ----
 
-template <int NDIM, int INTERP>
+template <int NDIM, int INTERP, int WIN>
 __global__ void __launch_bounds__(kThreads) project_kernel(
+    const float2* __restrict__ rec, const float* __restrict__ rot,
+    const float* __restrict__ shift, float2* __restrict__ out, Geom g, long long n_items)
+{
+    extern __shared__ int smem[];
+    int* rowstart = smem;                    // [Do + 1]
+    int* qslots = smem + g.Do + 1;           // [kQueue]
+    __shared__ int scratch[kThreads / 32];
+    __shared__ int qcount;
+    build_rowstart(g, rowstart, scratch);
+    if (threadIdx.x == 0) qcount = 0;
+    __syncthreads();
+    const Queue q{qslots, &qcount};
+    const int nkept = rowstart[g.Do];
+    const int npix = (int)g.img_elems;
+
+    for (long long item = blockIdx.x; item < n_items; item += gridDim.x) {
+        const ItemRange ir = item_of(g, item, 1);
+        ItemParams<NDIM> ip;
+        load_item<NDIM>(g, rot, shift, ir.r, ir.p, ip);
+        const float2* V = rec + (long long)ir.r * g.rec_elems;
+        float2* y = out + ir.item * g.img_elems;
+        // pixels beyond the cutoff are zero
+        for (int p = threadIdx.x; p < npix; p += kThreads) {
+            int i, j;
+            split_pixel(p, g.Ho, i, j);
+            if (j >= rowstart[i + 1] - rowstart[i]) y[p] = make_float2(0.f, 0.f);
+        }
+        auto finish = [&](int row, int kx, float2 val) {
+            const int ky = row_freq(row, g.Do, g.halfo, g.centered);
+            if (g.has_shift)
+                val = cmul(val, shift_phase((float)kx, (float)ky, ip.sx, ip.sy, g.Do_f, g.inv_Do));
+            y[row * g.Ho + kx] = val;
+        };
+        int row = 0;
+        for (int base = 0; base < nkept; base += kThreads) {
+            const int n = base + threadIdx.x;
+            bool slow = false;
+            int kx = 0;
+            if (n < nkept) {
+                while (rowstart[row + 1] <= n) ++row;
+                kx = n - rowstart[row];
+                const int ky = row_freq(row, g.Do, g.halfo, g.centered);
+                float2 v;
+                if (eval_fast<NDIM, INTERP, WIN, false>(g, V, ip.R, kx, ky, v, nullptr))
+                    finish(row, kx, v);
+                else
+                    slow = true;
+            }
+            enqueue(q, slow, row, kx);
+            __syncthreads();
+            if (qcount >= kThreads) {
+                const int e = q.slots[qcount - kThreads + threadIdx.x];
+                const int qrow = e >> 16, qkx = e & 0xffff;
+                float2 v;
+                eval_general<NDIM, INTERP, false>(g, V, ip.R, qkx,
+                                                  row_freq(qrow, g.Do, g.halfo, g.centered), v, nullptr);
+                finish(qrow, qkx, v);
+                __syncthreads();
+                if (threadIdx.x == 0) qcount -= kThreads;
+                __syncthreads();
+            }
+        }
+        if (threadIdx.x < qcount) {
+            const int e = q.slots[threadIdx.x];
+            const int qrow = e >> 16, qkx = e & 0xffff;
+            float2 v;
+            eval_general<NDIM, INTERP, false>(g, V, ip.R, qkx,
+                                              row_freq(qrow, g.Do, g.halfo, g.centered), v, nullptr);
+            finish(qrow, qkx, v);
+        }
+        __syncthreads();
+        if (threadIdx.x == 0) qcount = 0;
+        __syncthreads();
+    }
+}
+
+// Any image size: one thread per pixel slot, exact per-tap rule (used when the image has
+// more rows than the kept-pixel table holds).
+template <int NDIM, int INTERP>
+__global__ void __launch_bounds__(kThreads) project_kernel_any(
     const float2* __restrict__ rec, const float* __restrict__ rot,
     const float* __restrict__ shift, float2* __restrict__ out, Geom g, int splits,
     long long n_work)
@@ -56,9 +271,7 @@ __global__ void __launch_bounds__(kThreads) project_kernel(
             const int ky = row_freq(i, g.Do, g.halfo, g.centered), kx = j;
             float2 val = make_float2(0.f, 0.f);
             if (kx * kx + ky * ky <= g.rc2) {
-                PixelTaps<NDIM, INTERP, false> t;
-                t.init(g, ip.R, (float)kx, (float)ky);
-                gather<NDIM, INTERP, false>(V, g, t, val, nullptr);
+                eval_general<NDIM, INTERP, false>(g, V, ip.R, kx, ky, val, nullptr);
                 if (g.has_shift)
                     val = cmul(val, shift_phase((float)kx, (float)ky, ip.sx, ip.sy, g.Do_f, g.inv_Do));
             }
@@ -67,31 +280,125 @@ __global__ void __launch_bounds__(kThreads) project_kernel(
     }
 }
 
-// ----------------------------------------------------------------- backward ----
+// ------------------------------------------------- rotation / shift gradients ----
 
-// Sum of a per-thread value over the CTA, valid in thread 0.
-__device__ __forceinline__ float block_sum(float v, float* red)
+// Per pixel: g' = g conj(phase); dL/dR[a][b] += o q_b Re(conj(g') dv/dc_a) and
+// dL/ds_b += (2 pi / Do) q_b Im(conj(g') v), with q = (kx, ky).
+template <int NDIM>
+__device__ __forceinline__ void accumulate_grad(float* acc, float2 gp, float2 v, const float2* dv,
+                                                int kx, int ky)
 {
 #pragma unroll
-    for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
-    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-    __syncthreads();
-    if (lane == 0) red[warp] = v;
-    __syncthreads();
-    float s = 0.f;
-    if (threadIdx.x == 0)
-        for (int k = 0; k < kThreads / 32; ++k) s += red[k];
-    return s;
+    for (int a = 0; a < NDIM; ++a) {
+        const float cr = gp.x * dv[a].x + gp.y * dv[a].y;
+        acc[2 * a] = fmaf(cr, (float)kx, acc[2 * a]);
+        acc[2 * a + 1] = fmaf(cr, (float)ky, acc[2 * a + 1]);
+    }
+    const float ci = gp.x * v.y - gp.y * v.x;
+    acc[2 * NDIM] = fmaf(ci, (float)kx, acc[2 * NDIM]);
+    acc[2 * NDIM + 1] = fmaf(ci, (float)ky, acc[2 * NDIM + 1]);
 }
 
-template <int NDIM, int INTERP, bool WANT_REC, bool WANT_GRAD>
-__global__ void __launch_bounds__(kThreads) backward_kernel(
+template <int NDIM, int INTERP, int WIN>
+__global__ void __launch_bounds__(kThreads) grad_pose_kernel(
     const float2* __restrict__ rec, const float* __restrict__ rot,
     const float* __restrict__ shift, const float2* __restrict__ gout,
-    float2* __restrict__ grec, float* __restrict__ grot, float* __restrict__ gsh, Geom g,
-    int splits, long long n_work)
+    float* __restrict__ grot, float* __restrict__ gsh, Geom g, long long n_items)
 {
-    constexpr int NG = NDIM * 2 + 2;  // dL/dR[a][0..1] for a < NDIM, then dL/ds[0..1]
+    constexpr int NG = NDIM * 2 + 2;
+    extern __shared__ int smem[];
+    int* rowstart = smem;
+    int* qslots = smem + g.Do + 1;
+    __shared__ int scratch[kThreads / 32];
+    __shared__ float red[kThreads / 32];
+    __shared__ int qcount;
+    build_rowstart(g, rowstart, scratch);
+    if (threadIdx.x == 0) qcount = 0;
+    __syncthreads();
+    const Queue q{qslots, &qcount};
+    const int nkept = rowstart[g.Do];
+
+    for (long long item = blockIdx.x; item < n_items; item += gridDim.x) {
+        const ItemRange ir = item_of(g, item, 1);
+        ItemParams<NDIM> ip;
+        load_item<NDIM>(g, rot, shift, ir.r, ir.p, ip);
+        const float2* V = rec + (long long)ir.r * g.rec_elems;
+        const float2* gy = gout + ir.item * g.img_elems;
+        float acc[NG];
+#pragma unroll
+        for (int k = 0; k < NG; ++k) acc[k] = 0.f;
+        auto add = [&](int row, int kx, float2 v, const float2* dv) {
+            const int ky = row_freq(row, g.Do, g.halfo, g.centered);
+            float2 gp = __ldg(gy + row * g.Ho + kx);
+            if (g.has_shift)
+                gp = cmul_conj(gp, shift_phase((float)kx, (float)ky, ip.sx, ip.sy, g.Do_f, g.inv_Do));
+            accumulate_grad<NDIM>(acc, gp, v, dv, kx, ky);
+        };
+        int row = 0;
+        for (int base = 0; base < nkept; base += kThreads) {
+            const int n = base + threadIdx.x;
+            bool slow = false;
+            int kx = 0;
+            if (n < nkept) {
+                while (rowstart[row + 1] <= n) ++row;
+                kx = n - rowstart[row];
+                const int ky = row_freq(row, g.Do, g.halfo, g.centered);
+                float2 v, dv[3];
+                if (eval_fast<NDIM, INTERP, WIN, true>(g, V, ip.R, kx, ky, v, dv))
+                    add(row, kx, v, dv);
+                else
+                    slow = true;
+            }
+            enqueue(q, slow, row, kx);
+            __syncthreads();
+            if (qcount >= kThreads) {
+                const int e = q.slots[qcount - kThreads + threadIdx.x];
+                const int qrow = e >> 16, qkx = e & 0xffff;
+                float2 v, dv[3];
+                eval_general<NDIM, INTERP, true>(g, V, ip.R, qkx,
+                                                 row_freq(qrow, g.Do, g.halfo, g.centered), v, dv);
+                add(qrow, qkx, v, dv);
+                __syncthreads();
+                if (threadIdx.x == 0) qcount -= kThreads;
+                __syncthreads();
+            }
+        }
+        if (threadIdx.x < qcount) {
+            const int e = q.slots[threadIdx.x];
+            const int qrow = e >> 16, qkx = e & 0xffff;
+            float2 v, dv[3];
+            eval_general<NDIM, INTERP, true>(g, V, ip.R, qkx,
+                                             row_freq(qrow, g.Do, g.halfo, g.centered), v, dv);
+            add(qrow, qkx, v, dv);
+        }
+        __syncthreads();
+        if (threadIdx.x == 0) qcount = 0;
+        // per-item sums; several reconstructions may share one pose's parameters
+        const long long ri = (long long)(g.rot_shared ? 0 : ir.r) * g.n_pose + ir.p;
+        const long long si = (long long)(g.sh_shared ? 0 : ir.r) * g.n_pose + ir.p;
+        const float two_pi_over_Do = 6.283185307179586f * g.inv_Do;
+#pragma unroll
+        for (int k = 0; k < NG; ++k) {
+            const float s = block_sum(acc[k], red);
+            if (threadIdx.x == 0) {
+                if (k < 2 * NDIM) {
+                    if (grot) atomicAdd(grot + ri * NDIM * NDIM + (k / 2) * NDIM + (k % 2), g.o * s);
+                } else if (gsh && g.has_shift) {
+                    atomicAdd(gsh + si * 2 + (k - 2 * NDIM), two_pi_over_Do * s);
+                }
+            }
+        }
+    }
+}
+
+// Any image size: general per-tap path, one thread per pixel slot.
+template <int NDIM, int INTERP>
+__global__ void __launch_bounds__(kThreads) grad_pose_kernel_any(
+    const float2* __restrict__ rec, const float* __restrict__ rot,
+    const float* __restrict__ shift, const float2* __restrict__ gout,
+    float* __restrict__ grot, float* __restrict__ gsh, Geom g, int splits, long long n_work)
+{
+    constexpr int NG = NDIM * 2 + 2;
     __shared__ float red[kThreads / 32];
     const int npix = (int)g.img_elems;
     for (long long w = blockIdx.x; w < n_work; w += gridDim.x) {
@@ -99,7 +406,6 @@ __global__ void __launch_bounds__(kThreads) backward_kernel(
         ItemParams<NDIM> ip;
         load_item<NDIM>(g, rot, shift, ir.r, ir.p, ip);
         const float2* V = rec + (long long)ir.r * g.rec_elems;
-        float2* G = WANT_REC ? grec + (long long)ir.r * g.rec_elems : nullptr;
         const float2* gy = gout + ir.item * g.img_elems;
         float acc[NG];
 #pragma unroll
@@ -109,40 +415,24 @@ __global__ void __launch_bounds__(kThreads) backward_kernel(
             split_pixel(pix, g.Ho, i, j);
             const int ky = row_freq(i, g.Do, g.halfo, g.centered), kx = j;
             if (kx * kx + ky * ky > g.rc2) continue;
-            float2 gp = __ldg(gy + pix);  // g' = g conj(phase)
+            float2 gp = __ldg(gy + pix);
             if (g.has_shift)
                 gp = cmul_conj(gp, shift_phase((float)kx, (float)ky, ip.sx, ip.sy, g.Do_f, g.inv_Do));
-            PixelTaps<NDIM, INTERP, WANT_GRAD> t;
-            t.init(g, ip.R, (float)kx, (float)ky);
-            if constexpr (WANT_GRAD) {
-                float2 v, dv[3];
-                gather<NDIM, INTERP, true>(V, g, t, v, dv);
-                // Re(conj(g') dv/dc_a) times q_b; Im(conj(g') v) times q_b for the shifts
-#pragma unroll
-                for (int a = 0; a < NDIM; ++a) {
-                    const float cr = gp.x * dv[a].x + gp.y * dv[a].y;
-                    acc[2 * a] = fmaf(cr, (float)kx, acc[2 * a]);
-                    acc[2 * a + 1] = fmaf(cr, (float)ky, acc[2 * a + 1]);
-                }
-                const float ci = gp.x * v.y - gp.y * v.x;
-                acc[2 * NDIM] = fmaf(ci, (float)kx, acc[2 * NDIM]);
-                acc[2 * NDIM + 1] = fmaf(ci, (float)ky, acc[2 * NDIM + 1]);
-            }
-            if constexpr (WANT_REC) scatter<NDIM, INTERP, WANT_GRAD>(G, nullptr, g, t, gp, 0.f);
+            float2 v, dv[3];
+            eval_general<NDIM, INTERP, true>(g, V, ip.R, kx, ky, v, dv);
+            accumulate_grad<NDIM>(acc, gp, v, dv, kx, ky);
         }
-        if constexpr (WANT_GRAD) {
-            const long long ri = (long long)(g.rot_shared ? 0 : ir.r) * g.n_pose + ir.p;
-            const long long si = (long long)(g.sh_shared ? 0 : ir.r) * g.n_pose + ir.p;
-            const float two_pi_over_Do = 6.283185307179586f * g.inv_Do;
+        const long long ri = (long long)(g.rot_shared ? 0 : ir.r) * g.n_pose + ir.p;
+        const long long si = (long long)(g.sh_shared ? 0 : ir.r) * g.n_pose + ir.p;
+        const float two_pi_over_Do = 6.283185307179586f * g.inv_Do;
 #pragma unroll
-            for (int k = 0; k < NG; ++k) {
-                const float s = block_sum(acc[k], red);
-                if (threadIdx.x == 0) {
-                    if (k < 2 * NDIM) {
-                        if (grot) atomicAdd(grot + ri * NDIM * NDIM + (k / 2) * NDIM + (k % 2), g.o * s);
-                    } else if (gsh && g.has_shift) {
-                        atomicAdd(gsh + si * 2 + (k - 2 * NDIM), two_pi_over_Do * s);
-                    }
+        for (int k = 0; k < NG; ++k) {
+            const float s = block_sum(acc[k], red);
+            if (threadIdx.x == 0) {
+                if (k < 2 * NDIM) {
+                    if (grot) atomicAdd(grot + ri * NDIM * NDIM + (k / 2) * NDIM + (k % 2), g.o * s);
+                } else if (gsh && g.has_shift) {
+                    atomicAdd(gsh + si * 2 + (k - 2 * NDIM), two_pi_over_Do * s);
                 }
             }
         }
@@ -151,6 +441,8 @@ __global__ void __launch_bounds__(kThreads) backward_kernel(
 
 // ------------------------------------------------------------ back-projection ----
 
+// Scatter of every kept pixel of every item (data g conj(phase) and / or real weights):
+// the transpose of the forward projection.  Used for the volume gradient too.
 template <int NDIM, int INTERP>
 __global__ void __launch_bounds__(kThreads) backproject_kernel(
     const float2* __restrict__ proj, const float* __restrict__ weights,
@@ -182,6 +474,538 @@ __global__ void __launch_bounds__(kThreads) backproject_kernel(
     }
 }
 
+// Owner-computes back-projection (see scatter.cuh).  A CTA takes one item at a time; its
+// threads own row segments of the volume (3D: rows (u_z, u_y); 2D: rows u_y) and gather
+// the item's contributions to them.  DATA: proj * conj(phase) into vout (complex);
+// WTS: the real per-pixel weights into wout.
+constexpr int kMaxScatterBox = 1024;
+
+template <int INTERP>
+struct SegMargin {
+    // Candidates have c_x within s of the segment [X0, X0 + W), so their taps lie in
+    // [X0 - ML + 1, X0 + W + ML - 1); one spare slot on each side absorbs rounding.
+    static constexpr int ML = INTERP == kCubic ? 5 : 3;
+    static constexpr int AW = kSegW + 2 * ML;
+};
+
+template <int NDIM, int INTERP, bool DATA, bool WTS>
+__global__ void __launch_bounds__(kThreads) scatter_rows_kernel(
+    const float2* __restrict__ proj, const float* __restrict__ wts,
+    const float* __restrict__ rot, const float* __restrict__ shift,
+    float2* __restrict__ vout, float* __restrict__ wout, Geom g, long long n_items)
+{
+    constexpr int NT = Taps<INTERP>::N;
+    constexpr int FIRST = Taps<INTERP>::first;
+    constexpr float S = INTERP == kCubic ? 2.0f : 1.0f;
+    constexpr int W = kSegW;
+    constexpr int ML = SegMargin<INTERP>::ML;
+    constexpr int AW = SegMargin<INTERP>::AW;
+    extern __shared__ __align__(16) unsigned char sm_raw[];
+    // [acc: AW x kThreads float2][wacc: AW x kThreads float][twx: Ho][twy: Do][kmax: Do]
+    // [rowtab: Dv+1][ylo: Dv]
+    float2* acc = reinterpret_cast<float2*>(sm_raw);
+    float* wacc = reinterpret_cast<float*>(acc + (DATA ? AW * kThreads : 0));
+    float2* twx = reinterpret_cast<float2*>(wacc + (WTS ? AW * kThreads : 0));
+    float2* twy = twx + g.Ho;
+    int* kmaxt = reinterpret_cast<int*>(twy + g.Do);
+    int* rowtab = kmaxt + g.Do;
+    int* ylo = rowtab + g.Dv + 1;
+    __shared__ int scratch[kThreads / 32];
+    __shared__ float Rs[9];
+    __shared__ float2 sh;
+
+    for (int j = 0; j < AW; ++j) {
+        if (DATA) acc[j * kThreads + threadIdx.x] = make_float2(0.f, 0.f);
+        if (WTS) wacc[j * kThreads + threadIdx.x] = 0.f;
+    }
+    // last kept kx of every image row (-1: none)
+    for (int i = threadIdx.x; i < g.Do; i += kThreads) {
+        const int ky = row_freq(i, g.Do, g.halfo, g.centered);
+        kmaxt[i] = row_kept(g, i) - 1;
+        (void)ky;
+    }
+    const float rho = sqrtf((float)g.rc2) + 1e-3f;
+
+    for (long long item = blockIdx.x; item < n_items; item += gridDim.x) {
+        const ItemRange ir = item_of(g, item, 1);
+        if (threadIdx.x < NDIM * NDIM) {
+            const long long ri = (long long)(g.rot_shared ? 0 : ir.r) * g.n_pose + ir.p;
+            Rs[threadIdx.x] = g.o * __ldg(rot + ri * NDIM * NDIM + threadIdx.x);
+        }
+        if (threadIdx.x == 0) {
+            sh = make_float2(0.f, 0.f);
+            if (g.has_shift) {
+                const long long si = (long long)(g.sh_shared ? 0 : ir.r) * g.n_pose + ir.p;
+                sh = make_float2(__ldg(shift + si * 2), __ldg(shift + si * 2 + 1));
+            }
+        }
+        __syncthreads();
+        // separable shift twiddles: conj(phase(kx, ky)) = conj(twx[kx]) * conj(twy[row])
+        if (DATA && g.has_shift) {
+            for (int k = threadIdx.x; k < g.Ho; k += kThreads) {
+                const float2 t = shift_phase((float)k, 0.f, sh.x, sh.y, g.Do_f, g.inv_Do);
+                twx[k] = make_float2(t.x, -t.y);
+            }
+            for (int i = threadIdx.x; i < g.Do; i += kThreads) {
+                const float2 t = shift_phase(0.f, (float)row_freq(i, g.Do, g.halfo, g.centered), sh.x,
+                                             sh.y, g.Do_f, g.inv_Do);
+                twy[i] = make_float2(t.x, -t.y);
+            }
+        }
+        // rows that can receive contributions
+        int nrows;
+        if constexpr (NDIM == 3) {
+            // per z plane, the y range of the slice's disk cut by the strip |c_z - u_z| < s
+            const int per = (g.Dv + kThreads - 1) / kThreads;
+            const int i0 = threadIdx.x * per;
+            int cnt[4] = {0, 0, 0, 0};
+            int sum = 0;
+            for (int k = 0; k < per && k < 4; ++k) {
+                const int iz = i0 + k;
+                if (iz >= g.Dv) break;
+                const float uz = (float)row_freq(iz, g.Dv, g.halfv, g.centered);
+                float lo, hi;
+                int y0 = 0, y1 = -1;
+                if (strip_range(Rs[6], Rs[7], Rs[3], Rs[4], uz, S, rho, lo, hi)) {
+                    y0 = max(-g.halfv, (int)floorf(lo - S) - 1);
+                    y1 = min(g.halfv - 1, (int)ceilf(hi + S) + 1);
+                }
+                ylo[iz] = y0;
+                cnt[k] = max(0, y1 - y0 + 1);
+                sum += cnt[k];
+            }
+            const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+            int inc = sum;
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) {
+                const int v = __shfl_up_sync(0xffffffffu, inc, o);
+                if (lane >= o) inc += v;
+            }
+            if (lane == 31) scratch[warp] = inc;
+            __syncthreads();
+            if (threadIdx.x == 0) {
+                int a = 0;
+                for (int w = 0; w < kThreads / 32; ++w) {
+                    const int t = scratch[w];
+                    scratch[w] = a;
+                    a += t;
+                }
+            }
+            __syncthreads();
+            int run = scratch[warp] + inc - sum;
+            for (int k = 0; k < per && k < 4; ++k) {
+                const int iz = i0 + k;
+                if (iz >= g.Dv) break;
+                rowtab[iz] = run;
+                run += cnt[k];
+            }
+            if (threadIdx.x == kThreads - 1) rowtab[g.Dv] = run;
+            __syncthreads();
+            nrows = rowtab[g.Dv];
+        } else {
+            float lo, hi;
+            int y0 = 0, y1 = -1;
+            if (strip_range(0.f, 0.f, Rs[2], Rs[3], 0.f, 1.f, rho, lo, hi)) {
+                y0 = max(-g.halfv, (int)floorf(lo - S) - 1);
+                y1 = min(g.halfv - 1, (int)ceilf(hi + S) + 1);
+            }
+            nrows = max(0, y1 - y0 + 1);
+            if (threadIdx.x == 0) ylo[0] = y0;
+            __syncthreads();
+        }
+        const float2* py = DATA ? proj + ir.item * g.img_elems : nullptr;
+        const float* pw = (WTS && wts) ? wts + ir.item * g.img_elems : nullptr;  // NULL: weight 1
+        float2* G = DATA ? vout + (long long)ir.r * g.rec_elems : nullptr;
+        float* Wt = WTS ? wout + (long long)ir.r * g.rec_elems : nullptr;
+        // In-plane geometry.  (c_y[, c_z]) = M q; the kx of the plane point with
+        // (c_y, c_z) = (u_y, u_z) tells which pixels (direct, kx >= 0, or mirrored) feed a row.
+        const float nx = Rs[2], ny = Rs[5], nz = Rs[8];
+        float mdet, kxa, kxb, ekx;  // kx* = kxa * u_y + kxb * u_z; ekx: half-extent in kx
+        if constexpr (NDIM == 3) {
+            mdet = Rs[3] * Rs[7] - Rs[4] * Rs[6];
+            kxa = Rs[7] / mdet;
+            kxb = -Rs[4] / mdet;
+            ekx = S * (fabsf(kxa) + fabsf(kxb)) + 1.0f;
+        } else {
+            mdet = 1.0f;
+            kxa = kxb = 0.f;
+            ekx = 3.0e38f;  // 2D rows take both sides
+        }
+        const bool sides_known = NDIM == 3 && fabsf(mdet) > 1e-3f;
+        // ky ranges of the parallelogram from each pair of strips: pairs (x,y), (x,z), (y,z)
+        int iz = 0;
+        for (int n = threadIdx.x; n < nrows; n += kThreads) {
+            int uz = 0, uy;
+            if constexpr (NDIM == 3) {
+                while (rowtab[iz + 1] <= n) ++iz;
+                uz = row_freq(iz, g.Dv, g.halfv, g.centered);
+                uy = ylo[iz] + (n - rowtab[iz]);
+            } else {
+                uy = ylo[0] + n;
+            }
+            const int iy = full_index(uy, g.Dv, g.halfv, g.centered);
+            const int izs = NDIM == 3 ? full_index(uz, g.Dv, g.halfv, g.centered) : 0;
+            const long long roff = ((long long)izs * g.Dv + iy) * g.Hv;
+            // x extent of the contributions to this row
+            int xlo = 0, xhi = g.halfv;
+            if constexpr (NDIM == 3) {
+                if (fabsf(nx) > 1e-4f) {
+                    // direct taps (c_x near xc) and mirrored ones (pixels with c_x near -xc,
+                    // target -t_x) both land within xc +- (delta + s)
+                    const float xc = -(ny * (float)uy + nz * (float)uz) / nx;
+                    const float dl = S * (fabsf(ny) + fabsf(nz)) / fabsf(nx) + S + 1.0f;
+                    xlo = max(0, (int)floorf(xc - dl));
+                    xhi = min(g.halfv, (int)ceilf(xc + dl));
+                }
+            } else {
+                float lo, hi;
+                if (strip_range(Rs[2], Rs[3], Rs[0], Rs[1], (float)uy, S, rho, lo, hi)) {
+                    // c_x of the direct pixels lies in [lo, hi]; the mirrored pixels (c_y near
+                    // -u_y) have -c_x in the same interval, by the symmetry q -> -q of the disk
+                    xlo = max(0, (int)floorf(lo - S) - 1);
+                    xhi = min(g.halfv, (int)ceilf(hi + S) + 1);
+                } else {
+                    xhi = -1;
+                }
+            }
+            // which sides can contribute: direct pixels sit near kx*, mirrored ones near -kx*
+            bool do_direct = true, do_mirror = true;
+            if (sides_known) {
+                const float ks = kxa * (float)uy + kxb * (float)uz;
+                do_direct = ks + ekx >= 0.f;
+                do_mirror = -ks + ekx >= 0.f;
+            }
+            for (int X0 = xlo; X0 <= xhi; X0 += W) {
+                const float xm = (float)X0 + 0.5f * (float)(W - 1);
+                const float xh = 0.5f * (float)(W - 1) + S;
+                for (int pass = 0; pass < 2; ++pass) {
+                    // pass 0: direct taps t = u; pass 1: mirrored taps t = -u (u_x >= 1)
+                    if (pass == 0 ? !do_direct : !do_mirror) continue;
+                    const float sg = pass ? -1.0f : 1.0f;
+                    const bool skip_x0 = pass == 1 && X0 == 0;  // x = 0 has no mirrored taps
+                    Strip st[3];
+                    st[0] = {Rs[0], Rs[1], sg * xm, xh};
+                    st[1] = {Rs[NDIM], Rs[NDIM + 1], sg * (float)uy, S};
+                    if constexpr (NDIM == 3) st[2] = {Rs[6], Rs[7], sg * (float)uz, S};
+                    for_each_line<NDIM>(st, g, kmaxt, [&](int ky, int irow, int k0, int k1) {
+                        const float fky = (float)ky;
+                        const float cx0 = Rs[1] * fky, cy0 = Rs[NDIM + 1] * fky;
+                        const float cz0 = NDIM == 3 ? Rs[7] * fky : 0.f;
+                        const float2* prow = DATA ? py + irow * g.Ho : nullptr;
+                        const float* wrow = pw ? pw + irow * g.Ho : nullptr;
+                        const float2 tyv = (DATA && g.has_shift) ? twy[irow] : make_float2(1.f, 0.f);
+                        for (int kx = k0; kx <= k1; ++kx) {
+                            const float fkx = (float)kx;
+                            const float cx = sg * fmaf(Rs[0], fkx, cx0);
+                            float w = kernel_w<INTERP>(sg * fmaf(Rs[NDIM], fkx, cy0) - (float)uy);
+                            if constexpr (NDIM == 3)
+                                w *= kernel_w<INTERP>(sg * fmaf(Rs[6], fkx, cz0) - (float)uz);
+                            float2 s = make_float2(0.f, 0.f);
+                            float sw = 0.f;
+                            if constexpr (DATA) {
+                                float2 v = __ldg(prow + kx);
+                                if (g.has_shift) v = cmul(v, cmul(twx[kx], tyv));
+                                s = make_float2(w * v.x, sg * w * v.y);  // conj when mirrored
+                            }
+                            if constexpr (WTS) sw = wrow ? w * __ldg(wrow + kx) : w;
+                            const float fl = floorf(cx);
+                            float wx[NT];
+                            weights<INTERP>(cx - fl, wx);
+                            int j0 = (int)fl + FIRST - X0 + ML;
+                            j0 = min(max(j0, 0), AW - NT);  // never outside the thread's slots
+#pragma unroll
+                            for (int k = 0; k < NT; ++k) {
+                                const float wk = (skip_x0 && j0 + k == ML) ? 0.f : wx[k];
+                                if constexpr (DATA) {
+                                    float2& a = acc[(j0 + k) * kThreads + threadIdx.x];
+                                    a.x = fmaf(wk, s.x, a.x);
+                                    a.y = fmaf(wk, s.y, a.y);
+                                }
+                                if constexpr (WTS) {
+                                    float& b = wacc[(j0 + k) * kThreads + threadIdx.x];
+                                    b = fmaf(wk, sw, b);
+                                }
+                            }
+                        }
+                    });
+                }
+                // add the finished segment to the volume and clear the accumulator
+                for (int j = 0; j < ML; ++j) {
+                    if (DATA) acc[j * kThreads + threadIdx.x] = make_float2(0.f, 0.f);
+                    if (WTS) wacc[j * kThreads + threadIdx.x] = 0.f;
+                    if (DATA) acc[(ML + W + j) * kThreads + threadIdx.x] = make_float2(0.f, 0.f);
+                    if (WTS) wacc[(ML + W + j) * kThreads + threadIdx.x] = 0.f;
+                }
+                const int nown = min(W, g.halfv - X0 + 1);
+                if constexpr (DATA) {
+                    for (int j = 0; j < nown;) {
+                        float2* dst = G + roff + X0 + j;
+                        float2& a = acc[(ML + j) * kThreads + threadIdx.x];
+                        if (j + 1 < nown && (reinterpret_cast<uintptr_t>(dst) & 15) == 0) {
+                            float2& b = acc[(ML + j + 1) * kThreads + threadIdx.x];
+                            if (a.x != 0.f || a.y != 0.f || b.x != 0.f || b.y != 0.f)
+                                atomicAdd(reinterpret_cast<float4*>(dst), make_float4(a.x, a.y, b.x, b.y));
+                            a = make_float2(0.f, 0.f);
+                            b = make_float2(0.f, 0.f);
+                            j += 2;
+                        } else {
+                            if (a.x != 0.f || a.y != 0.f) atomicAdd(dst, a);
+                            a = make_float2(0.f, 0.f);
+                            j += 1;
+                        }
+                    }
+                    for (int j = nown; j < W; ++j) acc[(ML + j) * kThreads + threadIdx.x] = make_float2(0.f, 0.f);
+                }
+                if constexpr (WTS) {
+                    for (int j = 0; j < W; ++j) {
+                        float& b = wacc[(ML + j) * kThreads + threadIdx.x];
+                        if (j < nown && b != 0.f) atomicAdd(Wt + roff + X0 + j, b);
+                        b = 0.f;
+                    }
+                }
+            }
+        }
+        __syncthreads();
+    }
+}
+
+// Warp-tile back-projection for 3D.  A warp takes a 4 x 4 tile of kept pixels of one item
+// and accumulates the tile's taps in a private box of shared memory that covers the tile's
+// footprint (the axis-aligned box of its taps in the effective frame, at most 9^3 voxels
+// for o = 1).  The warp walks the tile's pixels one at a time with its lanes on the
+// pixel's taps (64 for cubic: two per lane); one pixel's taps are distinct voxels, so the
+// lanes read-modify-write shared memory without atomics and __syncwarp orders successive
+// pixels.  The finished box is added to the volume with coalesced vector reductions, one
+// per voxel touched by the tile instead of one per tap.  Pixels with c_x < 0 are handled in
+// the effective frame (c' = -c, conjugate value; see gather.cuh) in a second pass over the
+// tile; taps that fall on the mirrored side of x = 0 (only near the x = 0 plane), and tiles
+// whose box would overflow (large oversampling), use direct vector atomics.
+constexpr int kTileCap = 768;   // voxels of one warp's box
+constexpr int kTilePix = 16;    // 4 x 4 pixels
+
+template <int INTERP, bool DATA, bool WTS>
+__global__ void __launch_bounds__(kThreads) scatter_tile_kernel(
+    const float2* __restrict__ proj, const float* __restrict__ wts,
+    const float* __restrict__ rot, const float* __restrict__ shift,
+    float2* __restrict__ vout, float* __restrict__ wout, Geom g, long long n_items)
+{
+    constexpr int NT = Taps<INTERP>::N;
+    constexpr int FIRST = Taps<INTERP>::first;
+    constexpr int T = NT * NT * NT;        // taps per pixel
+    constexpr int LPP = T < 32 ? T : 32;   // lanes per pixel
+    constexpr int TPL = T / LPP;           // taps per lane
+    constexpr int NWARP = kThreads / 32;
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    extern __shared__ __align__(16) unsigned char sm_raw[];
+    // per warp: acc[kTileCap] float2 | wacc[kTileCap] float | records
+    constexpr int NREC = 3 * NT + 7;  // wx[NT] wy[NT] wz[NT] | gx gy | wt | base | fx fy fz
+    float2* acc = reinterpret_cast<float2*>(sm_raw) + warp * (DATA ? kTileCap : 0);
+    float* wacc = reinterpret_cast<float*>(reinterpret_cast<float2*>(sm_raw) + NWARP * (DATA ? kTileCap : 0)) +
+                  warp * (WTS ? kTileCap : 0);
+    float* recs = reinterpret_cast<float*>(reinterpret_cast<float2*>(sm_raw) + NWARP * (DATA ? kTileCap : 0)) +
+                  NWARP * (WTS ? kTileCap : 0) + warp * NREC * kTilePix;
+    int* reci = reinterpret_cast<int*>(recs);
+    __shared__ float Rs[9];
+    __shared__ float2 sh;
+
+    for (int e = lane; e < kTileCap; e += 32) {
+        if (DATA) acc[e] = make_float2(0.f, 0.f);
+        if (WTS) wacc[e] = 0.f;
+    }
+    // this lane's taps: tap index q = lane + 32 m -> (a, b, k) = (z, y, x) offsets
+    int ta[TPL], tb[TPL], tk[TPL];
+#pragma unroll
+    for (int m = 0; m < TPL; ++m) {
+        const int q = lane + 32 * m;
+        ta[m] = q / (NT * NT);
+        tb[m] = (q / NT) % NT;
+        tk[m] = q % NT;
+    }
+    const bool tap_lane = lane < LPP;
+    const int tiles_x = (g.Ho + 3) / 4, tiles_y = (g.Do + 3) / 4;
+    const int ntiles = tiles_x * tiles_y;
+
+    for (long long item = blockIdx.x; item < n_items; item += gridDim.x) {
+        const ItemRange ir = item_of(g, item, 1);
+        __syncthreads();
+        if (threadIdx.x < 9) {
+            const long long ri = (long long)(g.rot_shared ? 0 : ir.r) * g.n_pose + ir.p;
+            Rs[threadIdx.x] = g.o * __ldg(rot + ri * 9 + threadIdx.x);
+        }
+        if (threadIdx.x == 0) {
+            sh = make_float2(0.f, 0.f);
+            if (g.has_shift) {
+                const long long si = (long long)(g.sh_shared ? 0 : ir.r) * g.n_pose + ir.p;
+                sh = make_float2(__ldg(shift + si * 2), __ldg(shift + si * 2 + 1));
+            }
+        }
+        __syncthreads();
+        const float2* py = DATA ? proj + ir.item * g.img_elems : nullptr;
+        const float* pw = (WTS && wts) ? wts + ir.item * g.img_elems : nullptr;  // NULL: weight 1
+        float2* G = DATA ? vout + (long long)ir.r * g.rec_elems : nullptr;
+        float* Wt = WTS ? wout + (long long)ir.r * g.rec_elems : nullptr;
+
+        for (int tile = warp; tile < ntiles; tile += NWARP) {
+            const int ti = tile / tiles_x, tj = tile - ti * tiles_x;
+            // ---- per-pixel set-up: lane l < 16 owns pixel (row 4 ti + l / 4, kx 4 tj + l % 4)
+            const int prow = 4 * ti + (lane >> 2), pkx = 4 * tj + (lane & 3);
+            bool kept = false;
+            int ky = 0;
+            float cx = 0.f, cy = 0.f, cz = 0.f;
+            if (lane < kTilePix && prow < g.Do && pkx < g.Ho) {
+                ky = row_freq(prow, g.Do, g.halfo, g.centered);
+                kept = pkx * pkx + ky * ky <= g.rc2;
+                const float fkx = (float)pkx, fky = (float)ky;
+                cx = fmaf(Rs[0], fkx, Rs[1] * fky);
+                cy = fmaf(Rs[3], fkx, Rs[4] * fky);
+                cz = fmaf(Rs[6], fkx, Rs[7] * fky);
+            }
+            const unsigned kept_mask = __ballot_sync(0xffffffffu, kept);
+            if (!kept_mask) continue;
+            const bool neg = cx < 0.f;
+            const unsigned neg_mask = __ballot_sync(0xffffffffu, kept && neg);
+            // value of the pixel: g' = g conj(phase), its weight
+            float2 gp = make_float2(0.f, 0.f);
+            float wt = 1.f;
+            if (kept) {
+                if (DATA) {
+                    gp = __ldg(py + prow * g.Ho + pkx);
+                    if (g.has_shift)
+                        gp = cmul_conj(gp, shift_phase((float)pkx, (float)ky, sh.x, sh.y, g.Do_f, g.inv_Do));
+                }
+                if (WTS && pw) wt = __ldg(pw + prow * g.Ho + pkx);
+            }
+            for (int pass = 0; pass < 2; ++pass) {
+                const unsigned pmask = pass ? neg_mask : (kept_mask & ~neg_mask);
+                if (!pmask) continue;
+                const bool mine = (pmask >> lane) & 1u;
+                const float sg = pass ? -1.f : 1.f;
+                // effective coordinates and tap origin
+                // clamped like floor_frac: beyond 2^23 every tap is outside any box, and the
+                // integer box extents below stay far from overflow (NaN clamps too)
+                const float lim = 8388608.0f;
+                const float ex = fminf(fmaxf(sg * cx, -lim), lim);
+                const float ey = fminf(fmaxf(sg * cy, -lim), lim);
+                const float ez = fminf(fmaxf(sg * cz, -lim), lim);
+                const float flx = floorf(ex), fly = floorf(ey), flz = floorf(ez);
+                const int fx = (int)flx, fy = (int)fly, fz = (int)flz;
+                // box of this pass's taps
+                const int big = 1 << 28;
+                const int x0 = __reduce_min_sync(0xffffffffu, mine ? fx : big) + FIRST;
+                const int y0 = __reduce_min_sync(0xffffffffu, mine ? fy : big) + FIRST;
+                const int z0 = __reduce_min_sync(0xffffffffu, mine ? fz : big) + FIRST;
+                const int x1 = __reduce_max_sync(0xffffffffu, mine ? fx : -big) + FIRST + NT - 1;
+                const int y1 = __reduce_max_sync(0xffffffffu, mine ? fy : -big) + FIRST + NT - 1;
+                const int z1 = __reduce_max_sync(0xffffffffu, mine ? fz : -big) + FIRST + NT - 1;
+                const int NX = x1 - x0 + 1, NY = y1 - y0 + 1, NZ = z1 - z0 + 1;
+                const bool boxed = NX <= kTileCap && NY <= kTileCap && NZ <= kTileCap &&
+                                   (long long)NX * NY * NZ <= kTileCap;
+                // records of this pass's pixels
+                if (mine) {
+                    float* r = recs + lane;
+                    float w[NT];
+                    weights<INTERP>(ex - flx, w);
+#pragma unroll
+                    for (int k = 0; k < NT; ++k) r[k * kTilePix] = w[k];
+                    weights<INTERP>(ey - fly, w);
+#pragma unroll
+                    for (int k = 0; k < NT; ++k) r[(NT + k) * kTilePix] = w[k];
+                    weights<INTERP>(ez - flz, w);
+#pragma unroll
+                    for (int k = 0; k < NT; ++k) r[(2 * NT + k) * kTilePix] = w[k];
+                    // effective value: conj(g') on the mirrored pass (weights are real)
+                    r[(3 * NT) * kTilePix] = gp.x;
+                    r[(3 * NT + 1) * kTilePix] = sg * gp.y;
+                    r[(3 * NT + 2) * kTilePix] = wt;
+                    reci[lane + (3 * NT + 3) * kTilePix] =
+                        ((fz + FIRST - z0) * NY + (fy + FIRST - y0)) * NX + (fx + FIRST - x0);
+                    reci[lane + (3 * NT + 4) * kTilePix] = fx;
+                    reci[lane + (3 * NT + 5) * kTilePix] = fy;
+                    reci[lane + (3 * NT + 6) * kTilePix] = fz;
+                }
+                __syncwarp();
+                int toff[TPL];
+#pragma unroll
+                for (int m = 0; m < TPL; ++m) toff[m] = (ta[m] * NY + tb[m]) * NX + tk[m];
+                // ---- scatter: one pixel at a time, lanes on its taps
+                for (unsigned pm = pmask; pm; pm &= pm - 1) {
+                    const int j = __ffs(pm) - 1;
+                    if (tap_lane) {
+                        const float* r = recs + j;
+                        const float2 gv = make_float2(r[(3 * NT) * kTilePix], r[(3 * NT + 1) * kTilePix]);
+                        const float wtv = r[(3 * NT + 2) * kTilePix];
+                        const int base = reci[j + (3 * NT + 3) * kTilePix];
+                        const int pfx = reci[j + (3 * NT + 4) * kTilePix];
+#pragma unroll
+                        for (int m = 0; m < TPL; ++m) {
+                            const float w = r[(2 * NT + ta[m]) * kTilePix] * r[(NT + tb[m]) * kTilePix] *
+                                            r[tk[m] * kTilePix];
+                            const int ux = pfx + FIRST + tk[m];
+                            const bool direct = ux >= 1 || (ux == 0 && pass == 0);
+                            if (direct && boxed) {
+                                const int e = base + toff[m];
+                                if (DATA) {
+                                    float2 a = acc[e];
+                                    a.x = fmaf(w, gv.x, a.x);
+                                    a.y = fmaf(w, gv.y, a.y);
+                                    acc[e] = a;
+                                }
+                                if (WTS) wacc[e] = fmaf(w, wtv, wacc[e]);
+                            } else {
+                                // direct target outside the box, or the mirrored side of x = 0:
+                                // target u (direct) or -u (mirrored, conjugate value)
+                                const int pfy = reci[j + (3 * NT + 5) * kTilePix];
+                                const int pfz = reci[j + (3 * NT + 6) * kTilePix];
+                                int vx = ux, vy = pfy + FIRST + tb[m], vz = pfz + FIRST + ta[m];
+                                float vim = gv.y;
+                                if (!direct) {
+                                    vx = -vx;
+                                    vy = -vy;
+                                    vz = -vz;
+                                    vim = -vim;
+                                }
+                                const int iy = full_index(vy, g.Dv, g.halfv, g.centered);
+                                const int iz = full_index(vz, g.Dv, g.halfv, g.centered);
+                                if (vx >= 0 && vx <= g.halfv && iy >= 0 && iz >= 0) {
+                                    const long long off = ((long long)iz * g.Dv + iy) * g.Hv + vx;
+                                    if (DATA) atomicAdd(G + off, make_float2(w * gv.x, w * vim));
+                                    if (WTS) atomicAdd(Wt + off, w * wtv);
+                                }
+                            }
+                        }
+                    }
+                    __syncwarp();
+                }
+                // ---- add the box to the volume (read and clear)
+                if (boxed) {
+                    const int nbox = NX * NY * NZ;
+                    const int nxy = NX * NY;
+                    for (int e = lane; e < nbox; e += 32) {
+                        const int ez_ = e / nxy, rem = e - ez_ * nxy;
+                        const int ey_ = rem / NX, ex2 = rem - ey_ * NX;
+                        const int ux = x0 + ex2, uy = y0 + ey_, uz = z0 + ez_;
+                        const int iy = full_index(uy, g.Dv, g.halfv, g.centered);
+                        const int iz = full_index(uz, g.Dv, g.halfv, g.centered);
+                        const bool ok = ux >= 0 && ux <= g.halfv && iy >= 0 && iz >= 0;
+                        const long long off = ((long long)iz * g.Dv + iy) * g.Hv + ux;
+                        if (DATA) {
+                            const float2 a = acc[e];
+                            if (ok && (a.x != 0.f || a.y != 0.f)) atomicAdd(G + off, a);
+                            acc[e] = make_float2(0.f, 0.f);
+                        }
+                        if (WTS) {
+                            const float b = wacc[e];
+                            if (ok && b != 0.f) atomicAdd(Wt + off, b);
+                            wacc[e] = 0.f;
+                        }
+                    }
+                }
+                __syncwarp();
+            }
+        }
+    }
+}
+
 // ------------------------------------------------------------------ launches ----
 
 struct LaunchShape {
@@ -207,42 +1031,159 @@ LaunchShape launch_shape(const Geom& g, int sms)
     return s;
 }
 
+// Table kernels: one CTA per item at a time, grid = a few waves of resident CTAs.
+struct TableShape {
+    unsigned grid;
+    size_t smem;
+};
+
+TableShape table_shape(const Geom& g, int sms)
+{
+    const long long n_items = (long long)g.n_rec * g.n_pose;
+    const long long cap = 16LL * sms;  // persistent-style: the table is built once per CTA
+    TableShape t;
+    t.grid = (unsigned)(n_items < cap ? n_items : cap);
+    t.smem = (size_t)(g.Do + 1 + kQueue) * sizeof(int);
+    return t;
+}
+
+bool use_table(const Geom& g) { return g.Do <= kMaxTableRows; }
+
+// Widest aligned window the volume layout allows: 32-byte windows need the z-plane
+// stride Dv * Hv to be a multiple of 4 elements (Dv % 4 == 0).
+int window_for(const Geom& g, int ndim) { return (ndim == 2 || g.Dv % 4 == 0) ? TP_GATHER_WIN : 2; }
+
+template <int NDIM, int INTERP, int WIN>
+void launch_project_table(const Geom& g, const float2* R, const float* rot, const float* shift,
+                          float2* Y, int sms, cudaStream_t stream)
+{
+    const TableShape t = table_shape(g, sms);
+    project_kernel<NDIM, INTERP, WIN><<<t.grid, kThreads, t.smem, stream>>>(
+        R, rot, shift, Y, g, (long long)g.n_rec * g.n_pose);
+}
+
+template <int NDIM, int INTERP>
+void launch_project_t(const Geom& g, const float2* R, const float* rot, const float* shift,
+                      float2* Y, int sms, cudaStream_t stream)
+{
+    if (!use_table(g)) {
+        const LaunchShape s = launch_shape(g, sms);
+        project_kernel_any<NDIM, INTERP><<<s.grid, kThreads, 0, stream>>>(R, rot, shift, Y, g,
+                                                                           s.splits, s.n_work);
+        return;
+    }
+    if (window_for(g, NDIM) == 4)
+        launch_project_table<NDIM, INTERP, 4>(g, R, rot, shift, Y, sms, stream);
+    else if (window_for(g, NDIM) == 2)
+        launch_project_table<NDIM, INTERP, 2>(g, R, rot, shift, Y, sms, stream);
+    else
+        launch_project_table<NDIM, INTERP, 1>(g, R, rot, shift, Y, sms, stream);
+}
+
+template <int NDIM, int INTERP, int WIN>
+void launch_grad_table(const Geom& g, const float2* R, const float* rot, const float* shift,
+                       const float2* G, float* grot, float* gsh, int sms, cudaStream_t stream)
+{
+    const TableShape t = table_shape(g, sms);
+    grad_pose_kernel<NDIM, INTERP, WIN><<<t.grid, kThreads, t.smem, stream>>>(
+        R, rot, shift, G, grot, gsh, g, (long long)g.n_rec * g.n_pose);
+}
+
+template <int NDIM, int INTERP>
+void launch_grad_t(const Geom& g, const float2* R, const float* rot, const float* shift,
+                   const float2* G, float* grot, float* gsh, int sms, cudaStream_t stream)
+{
+    if (!use_table(g)) {
+        const LaunchShape s = launch_shape(g, sms);
+        grad_pose_kernel_any<NDIM, INTERP><<<s.grid, kThreads, 0, stream>>>(
+            R, rot, shift, G, grot, gsh, g, s.splits, s.n_work);
+        return;
+    }
+    if (window_for(g, NDIM) == 4)
+        launch_grad_table<NDIM, INTERP, 4>(g, R, rot, shift, G, grot, gsh, sms, stream);
+    else if (window_for(g, NDIM) == 2)
+        launch_grad_table<NDIM, INTERP, 2>(g, R, rot, shift, G, grot, gsh, sms, stream);
+    else
+        launch_grad_table<NDIM, INTERP, 1>(g, R, rot, shift, G, grot, gsh, sms, stream);
+}
+
+template <int NDIM, int INTERP, bool DATA, bool WTS>
+void launch_scatter_rows(const Geom& g, const float2* P, const float* weights, const float* rot,
+                         const float* shift, float2* VO, float* WO, int sms, cudaStream_t stream)
+{
+    constexpr int AW = SegMargin<INTERP>::AW;
+    const size_t smem = (DATA ? (size_t)AW * kThreads * 8 : 0) + (WTS ? (size_t)AW * kThreads * 4 : 0) +
+                        (size_t)(g.Ho + g.Do) * 8 + (size_t)(g.Do + 2 * g.Dv + 1) * 4;
+    auto kern = scatter_rows_kernel<NDIM, INTERP, DATA, WTS>;
+    cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    const long long n_items = (long long)g.n_rec * g.n_pose;
+    const long long cap = 8LL * sms;
+    const unsigned grid = (unsigned)(n_items < cap ? n_items : cap);
+    kern<<<grid, kThreads, smem, stream>>>(P, weights, rot, shift, VO, WO, g, n_items);
+}
+
+template <int INTERP, bool DATA, bool WTS>
+void launch_scatter_tile(const Geom& g, const float2* P, const float* weights, const float* rot,
+                         const float* shift, float2* VO, float* WO, int sms, cudaStream_t stream)
+{
+    constexpr int NT = Taps<INTERP>::N;
+    constexpr int NREC = 3 * NT + 7;
+    const size_t per_warp = (DATA ? (size_t)kTileCap * 8 : 0) + (WTS ? (size_t)kTileCap * 4 : 0) +
+                            (size_t)NREC * kTilePix * 4;
+    const size_t smem = per_warp * (kThreads / 32);
+    auto kern = scatter_tile_kernel<INTERP, DATA, WTS>;
+    cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    const long long n_items = (long long)g.n_rec * g.n_pose;
+    const long long cap = 8LL * sms;
+    const unsigned grid = (unsigned)(n_items < cap ? n_items : cap);
+    kern<<<grid, kThreads, smem, stream>>>(P, weights, rot, shift, VO, WO, g, n_items);
+}
+
+template <int NDIM, int INTERP>
+void launch_backproject_t(const Geom& g, const float2* P, const float* weights, const float* rot,
+                          const float* shift, float2* VO, float* WO, int sms, cudaStream_t stream)
+{
+    if (g.Dv > kMaxScatterBox || g.Do > kMaxScatterBox) {
+        const LaunchShape s = launch_shape(g, sms);
+        backproject_kernel<NDIM, INTERP><<<s.grid, kThreads, 0, stream>>>(P, weights, rot, shift, VO,
+                                                                           WO, g, s.splits, s.n_work);
+        return;
+    }
+    if constexpr (NDIM == 3) {
+        if (VO && WO)
+            launch_scatter_tile<INTERP, true, true>(g, P, weights, rot, shift, VO, WO, sms, stream);
+        else if (VO)
+            launch_scatter_tile<INTERP, true, false>(g, P, weights, rot, shift, VO, WO, sms, stream);
+        else
+            launch_scatter_tile<INTERP, false, true>(g, P, weights, rot, shift, VO, WO, sms, stream);
+        return;
+    }
+    if (VO && WO)
+        launch_scatter_rows<NDIM, INTERP, true, true>(g, P, weights, rot, shift, VO, WO, sms, stream);
+    else if (VO)
+        launch_scatter_rows<NDIM, INTERP, true, false>(g, P, weights, rot, shift, VO, WO, sms, stream);
+    else
+        launch_scatter_rows<NDIM, INTERP, false, true>(g, P, weights, rot, shift, VO, WO, sms, stream);
+}
+
 }  // namespace
 
 cudaError_t launch_project(int ndim, int interp, const Geom& g, const void* rec,
                            const float* rot, const float* shift, void* out, int sms,
                            cudaStream_t stream)
 {
-    const LaunchShape s = launch_shape(g, sms);
-    if (s.n_work == 0) return cudaSuccess;
+    if ((long long)g.n_rec * g.n_pose == 0) return cudaSuccess;
     auto R = static_cast<const float2*>(rec);
     auto Y = static_cast<float2*>(out);
     if (ndim == 3 && interp == kCubic)
-        project_kernel<3, kCubic><<<s.grid, kThreads, 0, stream>>>(R, rot, shift, Y, g, s.splits, s.n_work);
+        launch_project_t<3, kCubic>(g, R, rot, shift, Y, sms, stream);
     else if (ndim == 3)
-        project_kernel<3, kLinear><<<s.grid, kThreads, 0, stream>>>(R, rot, shift, Y, g, s.splits, s.n_work);
+        launch_project_t<3, kLinear>(g, R, rot, shift, Y, sms, stream);
     else if (interp == kCubic)
-        project_kernel<2, kCubic><<<s.grid, kThreads, 0, stream>>>(R, rot, shift, Y, g, s.splits, s.n_work);
+        launch_project_t<2, kCubic>(g, R, rot, shift, Y, sms, stream);
     else
-        project_kernel<2, kLinear><<<s.grid, kThreads, 0, stream>>>(R, rot, shift, Y, g, s.splits, s.n_work);
+        launch_project_t<2, kLinear>(g, R, rot, shift, Y, sms, stream);
     return cudaGetLastError();
-}
-
-template <int NDIM, int INTERP>
-static void launch_backward_t(const LaunchShape& s, const Geom& g, const float2* R,
-                              const float* rot, const float* shift, const float2* G,
-                              float2* grec, float* grot, float* gsh, cudaStream_t stream)
-{
-    const bool want_grad = grot || (gsh && g.has_shift);
-    if (grec && want_grad)
-        backward_kernel<NDIM, INTERP, true, true><<<s.grid, kThreads, 0, stream>>>(
-            R, rot, shift, G, grec, grot, gsh, g, s.splits, s.n_work);
-    else if (grec)
-        backward_kernel<NDIM, INTERP, true, false><<<s.grid, kThreads, 0, stream>>>(
-            R, rot, shift, G, grec, grot, gsh, g, s.splits, s.n_work);
-    else if (want_grad)
-        backward_kernel<NDIM, INTERP, false, true><<<s.grid, kThreads, 0, stream>>>(
-            R, rot, shift, G, grec, grot, gsh, g, s.splits, s.n_work);
 }
 
 cudaError_t launch_backward(int ndim, int interp, const Geom& g, const void* rec,
@@ -250,19 +1191,31 @@ cudaError_t launch_backward(int ndim, int interp, const Geom& g, const void* rec
                             void* grad_rec, float* grad_rot, float* grad_shift, int sms,
                             cudaStream_t stream)
 {
-    const LaunchShape s = launch_shape(g, sms);
-    if (s.n_work == 0) return cudaSuccess;
+    if ((long long)g.n_rec * g.n_pose == 0) return cudaSuccess;
     auto R = static_cast<const float2*>(rec);
     auto G = static_cast<const float2*>(grad_out);
     auto GR = static_cast<float2*>(grad_rec);
-    if (ndim == 3 && interp == kCubic)
-        launch_backward_t<3, kCubic>(s, g, R, rot, shift, G, GR, grad_rot, grad_shift, stream);
-    else if (ndim == 3)
-        launch_backward_t<3, kLinear>(s, g, R, rot, shift, G, GR, grad_rot, grad_shift, stream);
-    else if (interp == kCubic)
-        launch_backward_t<2, kCubic>(s, g, R, rot, shift, G, GR, grad_rot, grad_shift, stream);
-    else
-        launch_backward_t<2, kLinear>(s, g, R, rot, shift, G, GR, grad_rot, grad_shift, stream);
+    const bool want_grad = grad_rot || (grad_shift && g.has_shift);
+    if (want_grad) {
+        if (ndim == 3 && interp == kCubic)
+            launch_grad_t<3, kCubic>(g, R, rot, shift, G, grad_rot, grad_shift, sms, stream);
+        else if (ndim == 3)
+            launch_grad_t<3, kLinear>(g, R, rot, shift, G, grad_rot, grad_shift, sms, stream);
+        else if (interp == kCubic)
+            launch_grad_t<2, kCubic>(g, R, rot, shift, G, grad_rot, grad_shift, sms, stream);
+        else
+            launch_grad_t<2, kLinear>(g, R, rot, shift, G, grad_rot, grad_shift, sms, stream);
+    }
+    if (GR) {
+        if (ndim == 3 && interp == kCubic)
+            launch_backproject_t<3, kCubic>(g, G, nullptr, rot, shift, GR, nullptr, sms, stream);
+        else if (ndim == 3)
+            launch_backproject_t<3, kLinear>(g, G, nullptr, rot, shift, GR, nullptr, sms, stream);
+        else if (interp == kCubic)
+            launch_backproject_t<2, kCubic>(g, G, nullptr, rot, shift, GR, nullptr, sms, stream);
+        else
+            launch_backproject_t<2, kLinear>(g, G, nullptr, rot, shift, GR, nullptr, sms, stream);
+    }
     return cudaGetLastError();
 }
 
@@ -270,18 +1223,17 @@ cudaError_t launch_backproject(int ndim, int interp, const Geom& g, const void* 
                                const float* weights, const float* rot, const float* shift,
                                void* vol_out, float* wvol_out, int sms, cudaStream_t stream)
 {
-    const LaunchShape s = launch_shape(g, sms);
-    if (s.n_work == 0 || (!vol_out && !wvol_out)) return cudaSuccess;
+    if ((long long)g.n_rec * g.n_pose == 0 || (!vol_out && !wvol_out)) return cudaSuccess;
     auto P = static_cast<const float2*>(proj);
     auto VO = static_cast<float2*>(vol_out);
     if (ndim == 3 && interp == kCubic)
-        backproject_kernel<3, kCubic><<<s.grid, kThreads, 0, stream>>>(P, weights, rot, shift, VO, wvol_out, g, s.splits, s.n_work);
+        launch_backproject_t<3, kCubic>(g, P, weights, rot, shift, VO, wvol_out, sms, stream);
     else if (ndim == 3)
-        backproject_kernel<3, kLinear><<<s.grid, kThreads, 0, stream>>>(P, weights, rot, shift, VO, wvol_out, g, s.splits, s.n_work);
+        launch_backproject_t<3, kLinear>(g, P, weights, rot, shift, VO, wvol_out, sms, stream);
     else if (interp == kCubic)
-        backproject_kernel<2, kCubic><<<s.grid, kThreads, 0, stream>>>(P, weights, rot, shift, VO, wvol_out, g, s.splits, s.n_work);
+        launch_backproject_t<2, kCubic>(g, P, weights, rot, shift, VO, wvol_out, sms, stream);
     else
-        backproject_kernel<2, kLinear><<<s.grid, kThreads, 0, stream>>>(P, weights, rot, shift, VO, wvol_out, g, s.splits, s.n_work);
+        launch_backproject_t<2, kLinear>(g, P, weights, rot, shift, VO, wvol_out, sms, stream);
     return cudaGetLastError();
 }
 

@@ -50,6 +50,8 @@ def parse():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-sample", type=int, default=1024, help="poses in the oracle sample")
+    ap.add_argument("--batch", type=int, default=None,
+                    help="override the workload's batch (small cases for profiling only)")
     return ap.parse_args()
 
 
@@ -386,7 +388,7 @@ def main():
         if rank != 0:
             return 0
         return run_reference(args, synth.make_workload(args.workload))
-    wl = synth.make_workload(args.workload)
+    wl = synth.make_workload(args.workload, B=args.batch)
     if wl.op != "fwdbwd" or wl.ndim != 3:
         raise SystemExit("bench.py times the 3D forward + backward workloads")
     return run_ours(args, wl)
