@@ -775,13 +775,31 @@ __global__ void __launch_bounds__(kThreads) scatter_rows_kernel(
 // for o = 1).  The warp walks the tile's pixels one at a time with its lanes on the
 // pixel's taps (64 for cubic: two per lane); one pixel's taps are distinct voxels, so the
 // lanes read-modify-write shared memory without atomics and __syncwarp orders successive
-// pixels.  The finished box is added to the volume with coalesced vector reductions, one
-// per voxel touched by the tile instead of one per tap.  Pixels with c_x < 0 are handled in
-// the effective frame (c' = -c, conjugate value; see gather.cuh) in a second pass over the
-// tile; taps that fall on the mirrored side of x = 0 (only near the x = 0 plane), and tiles
-// whose box would overflow (large oversampling), use direct vector atomics.
-constexpr int kTileCap = 768;   // voxels of one warp's box
-constexpr int kTilePix = 16;    // 4 x 4 pixels
+// pixels.  The box rows have a pitch of 12 voxels: a half-warp's 16 taps (4 y rows x 4 x
+// taps, 8-byte values) then fall in 16 distinct bank pairs.  The finished box is added to
+// the volume with coalesced vector reductions, one per voxel touched by the tile instead
+// of one per tap.  Pixels with c_x < 0 are handled in the effective frame (c' = -c,
+// conjugate value; see gather.cuh) in a second pass over the tile; pixels whose taps reach
+// the x <= 0 planes take the exact per-tap rule, and tiles whose box would overflow (large
+// oversampling) use direct vector atomics.
+constexpr int kBoxPitch = 12;
+constexpr int kBoxRows = 81;                        // NY * NZ <= 9 * 9
+constexpr int kTileCap = kBoxPitch * kBoxRows;      // voxels of one warp's box
+constexpr int kTilePix = 16;                        // 4 x 4 pixels
+
+template <int INTERP>
+struct TileRec {
+    static constexpr int NT = Taps<INTERP>::N;
+    // One record per pixel, stored contiguously (array of structs, odd stride) so that the
+    // lanes reading different fields of one pixel hit different banks:
+    // wzy[NT*NT] | wx[NT] | wt | gx gy | base fx fy fz (ints; base < 0 flags the
+    // per-tap path and holds ~base)
+    static constexpr int WZY = 0, WX = NT * NT, WT = NT * NT + NT, GX = WT + 1, GY = WT + 2;
+    static constexpr int BASE = WT + 3, FX = WT + 4, FY = WT + 5, FZ = WT + 6;
+    static constexpr int USED = WT + 7;
+    static constexpr int STRIDE = USED | 1;
+    static constexpr int WORDS = STRIDE * kTilePix > kBoxRows ? STRIDE * kTilePix : kBoxRows;
+};
 
 template <int INTERP, bool DATA, bool WTS>
 __global__ void __launch_bounds__(kThreads) scatter_tile_kernel(
@@ -789,6 +807,7 @@ __global__ void __launch_bounds__(kThreads) scatter_tile_kernel(
     const float* __restrict__ rot, const float* __restrict__ shift,
     float2* __restrict__ vout, float* __restrict__ wout, Geom g, long long n_items)
 {
+    using TR = TileRec<INTERP>;
     constexpr int NT = Taps<INTERP>::N;
     constexpr int FIRST = Taps<INTERP>::first;
     constexpr int T = NT * NT * NT;        // taps per pixel
@@ -797,14 +816,14 @@ __global__ void __launch_bounds__(kThreads) scatter_tile_kernel(
     constexpr int NWARP = kThreads / 32;
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     extern __shared__ __align__(16) unsigned char sm_raw[];
-    // per warp: acc[kTileCap] float2 | wacc[kTileCap] float | records
-    constexpr int NREC = 3 * NT + 7;  // wx[NT] wy[NT] wz[NT] | gx gy | wt | base | fx fy fz
+    // per warp: acc[kTileCap] float2 | wacc[kTileCap] float | records (TR::WORDS words)
     float2* acc = reinterpret_cast<float2*>(sm_raw) + warp * (DATA ? kTileCap : 0);
     float* wacc = reinterpret_cast<float*>(reinterpret_cast<float2*>(sm_raw) + NWARP * (DATA ? kTileCap : 0)) +
                   warp * (WTS ? kTileCap : 0);
-    float* recs = reinterpret_cast<float*>(reinterpret_cast<float2*>(sm_raw) + NWARP * (DATA ? kTileCap : 0)) +
-                  NWARP * (WTS ? kTileCap : 0) + warp * NREC * kTilePix;
-    int* reci = reinterpret_cast<int*>(recs);
+    float* recf = reinterpret_cast<float*>(reinterpret_cast<float2*>(sm_raw) + NWARP * (DATA ? kTileCap : 0)) +
+                  NWARP * (WTS ? kTileCap : 0) + warp * TR::WORDS;
+    int* reci = reinterpret_cast<int*>(recf);
+    int* rowoff = reci;  // reused after the pixel loop: global row offsets of the box rows
     __shared__ float Rs[9];
     __shared__ float2 sh;
 
@@ -813,13 +832,13 @@ __global__ void __launch_bounds__(kThreads) scatter_tile_kernel(
         if (WTS) wacc[e] = 0.f;
     }
     // this lane's taps: tap index q = lane + 32 m -> (a, b, k) = (z, y, x) offsets
-    int ta[TPL], tb[TPL], tk[TPL];
+    int ta[TPL], tb[TPL];
+    const int tk = lane % NT;
 #pragma unroll
     for (int m = 0; m < TPL; ++m) {
         const int q = lane + 32 * m;
         ta[m] = q / (NT * NT);
         tb[m] = (q / NT) % NT;
-        tk[m] = q % NT;
     }
     const bool tap_lane = lane < LPP;
     const int tiles_x = (g.Ho + 3) / 4, tiles_y = (g.Do + 3) / 4;
@@ -880,9 +899,8 @@ __global__ void __launch_bounds__(kThreads) scatter_tile_kernel(
                 if (!pmask) continue;
                 const bool mine = (pmask >> lane) & 1u;
                 const float sg = pass ? -1.f : 1.f;
-                // effective coordinates and tap origin
-                // clamped like floor_frac: beyond 2^23 every tap is outside any box, and the
-                // integer box extents below stay far from overflow (NaN clamps too)
+                // effective coordinates, clamped like floor_frac: beyond 2^23 every tap is
+                // outside any box and the integer extents below stay far from overflow
                 const float lim = 8388608.0f;
                 const float ex = fminf(fmaxf(sg * cx, -lim), lim);
                 const float ey = fminf(fmaxf(sg * cy, -lim), lim);
@@ -898,51 +916,51 @@ __global__ void __launch_bounds__(kThreads) scatter_tile_kernel(
                 const int y1 = __reduce_max_sync(0xffffffffu, mine ? fy : -big) + FIRST + NT - 1;
                 const int z1 = __reduce_max_sync(0xffffffffu, mine ? fz : -big) + FIRST + NT - 1;
                 const int NX = x1 - x0 + 1, NY = y1 - y0 + 1, NZ = z1 - z0 + 1;
-                const bool boxed = NX <= kTileCap && NY <= kTileCap && NZ <= kTileCap &&
-                                   (long long)NX * NY * NZ <= kTileCap;
+                const bool boxed = NX <= kBoxPitch && NY <= kBoxRows && NZ <= kBoxRows &&
+                                   NY * NZ <= kBoxRows;
                 // records of this pass's pixels
                 if (mine) {
-                    float* r = recs + lane;
-                    float w[NT];
-                    weights<INTERP>(ex - flx, w);
+                    float wx_[NT], wy_[NT], wz_[NT];
+                    weights<INTERP>(ex - flx, wx_);
+                    weights<INTERP>(ey - fly, wy_);
+                    weights<INTERP>(ez - flz, wz_);
+                    float* rf = recf + lane * TR::STRIDE;
+                    int* ri = reci + lane * TR::STRIDE;
 #pragma unroll
-                    for (int k = 0; k < NT; ++k) r[k * kTilePix] = w[k];
-                    weights<INTERP>(ey - fly, w);
+                    for (int a = 0; a < NT; ++a)
 #pragma unroll
-                    for (int k = 0; k < NT; ++k) r[(NT + k) * kTilePix] = w[k];
-                    weights<INTERP>(ez - flz, w);
+                        for (int b = 0; b < NT; ++b) rf[TR::WZY + a * NT + b] = wz_[a] * wy_[b];
 #pragma unroll
-                    for (int k = 0; k < NT; ++k) r[(2 * NT + k) * kTilePix] = w[k];
+                    for (int k = 0; k < NT; ++k) rf[TR::WX + k] = wx_[k];
+                    rf[TR::WT] = wt;
                     // effective value: conj(g') on the mirrored pass (weights are real)
-                    r[(3 * NT) * kTilePix] = gp.x;
-                    r[(3 * NT + 1) * kTilePix] = sg * gp.y;
-                    r[(3 * NT + 2) * kTilePix] = wt;
-                    reci[lane + (3 * NT + 3) * kTilePix] =
-                        ((fz + FIRST - z0) * NY + (fy + FIRST - y0)) * NX + (fx + FIRST - x0);
-                    reci[lane + (3 * NT + 4) * kTilePix] = fx;
-                    reci[lane + (3 * NT + 5) * kTilePix] = fy;
-                    reci[lane + (3 * NT + 6) * kTilePix] = fz;
+                    rf[TR::GX] = gp.x;
+                    rf[TR::GY] = sg * gp.y;
+                    const int base = ((fz + FIRST - z0) * NY + (fy + FIRST - y0)) * kBoxPitch + (fx + FIRST - x0);
+                    ri[TR::BASE] = (fx + FIRST <= 0 || !boxed) ? ~base : base;
+                    ri[TR::FX] = fx;
+                    ri[TR::FY] = fy;
+                    ri[TR::FZ] = fz;
                 }
                 __syncwarp();
                 int toff[TPL];
 #pragma unroll
-                for (int m = 0; m < TPL; ++m) toff[m] = (ta[m] * NY + tb[m]) * NX + tk[m];
+                for (int m = 0; m < TPL; ++m) toff[m] = (ta[m] * NY + tb[m]) * kBoxPitch + tk;
                 // ---- scatter: one pixel at a time, lanes on its taps
                 for (unsigned pm = pmask; pm; pm &= pm - 1) {
                     const int j = __ffs(pm) - 1;
                     if (tap_lane) {
-                        const float* r = recs + j;
-                        const float2 gv = make_float2(r[(3 * NT) * kTilePix], r[(3 * NT + 1) * kTilePix]);
-                        const float wtv = r[(3 * NT + 2) * kTilePix];
-                        const int base = reci[j + (3 * NT + 3) * kTilePix];
-                        const int pfx = reci[j + (3 * NT + 4) * kTilePix];
+                        const float* rf = recf + j * TR::STRIDE;
+                        const int* ri = reci + j * TR::STRIDE;
+                        const float2 gv = make_float2(rf[TR::GX], rf[TR::GY]);
+                        const float wtv = WTS ? rf[TR::WT] : 0.f;
+                        const float wxk = rf[TR::WX + tk];
+                        const int rb = ri[TR::BASE];
+                        const int base = rb < 0 ? ~rb : rb;
+                        if (rb >= 0) {
 #pragma unroll
-                        for (int m = 0; m < TPL; ++m) {
-                            const float w = r[(2 * NT + ta[m]) * kTilePix] * r[(NT + tb[m]) * kTilePix] *
-                                            r[tk[m] * kTilePix];
-                            const int ux = pfx + FIRST + tk[m];
-                            const bool direct = ux >= 1 || (ux == 0 && pass == 0);
-                            if (direct && boxed) {
+                            for (int m = 0; m < TPL; ++m) {
+                                const float w = rf[TR::WZY + ta[m] * NT + tb[m]] * wxk;
                                 const int e = base + toff[m];
                                 if (DATA) {
                                     float2 a = acc[e];
@@ -951,25 +969,43 @@ __global__ void __launch_bounds__(kThreads) scatter_tile_kernel(
                                     acc[e] = a;
                                 }
                                 if (WTS) wacc[e] = fmaf(w, wtv, wacc[e]);
-                            } else {
-                                // direct target outside the box, or the mirrored side of x = 0:
-                                // target u (direct) or -u (mirrored, conjugate value)
-                                const int pfy = reci[j + (3 * NT + 5) * kTilePix];
-                                const int pfz = reci[j + (3 * NT + 6) * kTilePix];
-                                int vx = ux, vy = pfy + FIRST + tb[m], vz = pfz + FIRST + ta[m];
-                                float vim = gv.y;
-                                if (!direct) {
-                                    vx = -vx;
-                                    vy = -vy;
-                                    vz = -vz;
-                                    vim = -vim;
-                                }
-                                const int iy = full_index(vy, g.Dv, g.halfv, g.centered);
-                                const int iz = full_index(vz, g.Dv, g.halfv, g.centered);
-                                if (vx >= 0 && vx <= g.halfv && iy >= 0 && iz >= 0) {
-                                    const long long off = ((long long)iz * g.Dv + iy) * g.Hv + vx;
-                                    if (DATA) atomicAdd(G + off, make_float2(w * gv.x, w * vim));
-                                    if (WTS) atomicAdd(Wt + off, w * wtv);
+                            }
+                        } else {
+                            // taps on the x <= 0 planes (exact per-tap rule), or no box
+                            const int pfx = ri[TR::FX];
+                            const int pfy = ri[TR::FY];
+                            const int pfz = ri[TR::FZ];
+#pragma unroll
+                            for (int m = 0; m < TPL; ++m) {
+                                const float w = rf[TR::WZY + ta[m] * NT + tb[m]] * wxk;
+                                const int ux = pfx + FIRST + tk;
+                                const bool direct = ux >= 1 || (ux == 0 && pass == 0);
+                                if (direct && boxed) {
+                                    const int e = base + toff[m];
+                                    if (DATA) {
+                                        float2 a = acc[e];
+                                        a.x = fmaf(w, gv.x, a.x);
+                                        a.y = fmaf(w, gv.y, a.y);
+                                        acc[e] = a;
+                                    }
+                                    if (WTS) wacc[e] = fmaf(w, wtv, wacc[e]);
+                                } else {
+                                    // target u (direct) or -u (mirrored, conjugate value)
+                                    int vx = ux, vy = pfy + FIRST + tb[m], vz = pfz + FIRST + ta[m];
+                                    float vim = gv.y;
+                                    if (!direct) {
+                                        vx = -vx;
+                                        vy = -vy;
+                                        vz = -vz;
+                                        vim = -vim;
+                                    }
+                                    const int iy = full_index(vy, g.Dv, g.halfv, g.centered);
+                                    const int iz = full_index(vz, g.Dv, g.halfv, g.centered);
+                                    if (vx >= 0 && vx <= g.halfv && iy >= 0 && iz >= 0) {
+                                        const long long off = ((long long)iz * g.Dv + iy) * g.Hv + vx;
+                                        if (DATA) atomicAdd(G + off, make_float2(w * gv.x, w * vim));
+                                        if (WTS) atomicAdd(Wt + off, w * wtv);
+                                    }
                                 }
                             }
                         }
@@ -978,24 +1014,29 @@ __global__ void __launch_bounds__(kThreads) scatter_tile_kernel(
                 }
                 // ---- add the box to the volume (read and clear)
                 if (boxed) {
-                    const int nbox = NX * NY * NZ;
-                    const int nxy = NX * NY;
+                    const int nrow = NY * NZ;
+                    for (int r = lane; r < nrow; r += 32) {
+                        const int zi = r / NY, yi = r - zi * NY;
+                        const int iy = full_index(y0 + yi, g.Dv, g.halfv, g.centered);
+                        const int iz = full_index(z0 + zi, g.Dv, g.halfv, g.centered);
+                        rowoff[r] = (iy < 0 || iz < 0) ? -1 : (iz * g.Dv + iy) * g.Hv;
+                    }
+                    __syncwarp();
+                    const int nbox = nrow * kBoxPitch;
                     for (int e = lane; e < nbox; e += 32) {
-                        const int ez_ = e / nxy, rem = e - ez_ * nxy;
-                        const int ey_ = rem / NX, ex2 = rem - ey_ * NX;
-                        const int ux = x0 + ex2, uy = y0 + ey_, uz = z0 + ez_;
-                        const int iy = full_index(uy, g.Dv, g.halfv, g.centered);
-                        const int iz = full_index(uz, g.Dv, g.halfv, g.centered);
-                        const bool ok = ux >= 0 && ux <= g.halfv && iy >= 0 && iz >= 0;
-                        const long long off = ((long long)iz * g.Dv + iy) * g.Hv + ux;
+                        const int r = (int)(((unsigned)e * 0xAAABu) >> 19);  // e / 12 for e < 2^15
+                        const int xi = e - r * kBoxPitch;
+                        const int ux = x0 + xi;
+                        const int ro = rowoff[r];
+                        const bool ok = xi < NX && ro >= 0 && ux >= 0 && ux <= g.halfv;
                         if (DATA) {
                             const float2 a = acc[e];
-                            if (ok && (a.x != 0.f || a.y != 0.f)) atomicAdd(G + off, a);
+                            if (ok && (a.x != 0.f || a.y != 0.f)) atomicAdd(G + ro + ux, a);
                             acc[e] = make_float2(0.f, 0.f);
                         }
                         if (WTS) {
                             const float b = wacc[e];
-                            if (ok && b != 0.f) atomicAdd(Wt + off, b);
+                            if (ok && b != 0.f) atomicAdd(Wt + ro + ux, b);
                             wacc[e] = 0.f;
                         }
                     }
@@ -1126,10 +1167,8 @@ template <int INTERP, bool DATA, bool WTS>
 void launch_scatter_tile(const Geom& g, const float2* P, const float* weights, const float* rot,
                          const float* shift, float2* VO, float* WO, int sms, cudaStream_t stream)
 {
-    constexpr int NT = Taps<INTERP>::N;
-    constexpr int NREC = 3 * NT + 7;
     const size_t per_warp = (DATA ? (size_t)kTileCap * 8 : 0) + (WTS ? (size_t)kTileCap * 4 : 0) +
-                            (size_t)NREC * kTilePix * 4;
+                            (size_t)TileRec<INTERP>::WORDS * 4;
     const size_t smem = per_warp * (kThreads / 32);
     auto kern = scatter_tile_kernel<INTERP, DATA, WTS>;
     cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);

@@ -37,7 +37,9 @@ METRIC = "projections/sec fwd+bwd at D=128 cubic; achieved GB/s vs HBM/L2 roofli
 DEFAULT_WORKLOAD = "fwdbwd3d_d128_cubic_b16384"
 TRAFFIC_FILE = ROOT / "profiles" / "traffic.json"
 KERNEL_SOURCES = ["back_projection_fourier_b300/csrc/kernels.cu",
-                  "back_projection_fourier_b300/csrc/tp_device.cuh"]
+                  "back_projection_fourier_b300/csrc/tp_device.cuh",
+                  "back_projection_fourier_b300/csrc/gather.cuh",
+                  "back_projection_fourier_b300/csrc/scatter.cuh"]
 
 
 def parse():
@@ -49,7 +51,7 @@ def parse():
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD)
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--cpu-sample", type=int, default=1024, help="poses in the oracle sample")
+    ap.add_argument("--cpu-sample", type=int, default=16384, help="poses in the oracle sample")
     ap.add_argument("--batch", type=int, default=None,
                     help="override the workload's batch (small cases for profiling only)")
     return ap.parse_args()
@@ -188,16 +190,18 @@ def workload_config(wl, l2: str) -> dict:
 
 
 def hbm_bytes(wl):
-    """Algorithmic HBM bytes per launch: each unique input read once, each output written
-    once.  Per projection: Do*(Do/2+1)*8 B of image (written by the forward, read by the
-    backward) plus 4*(k*k+2) B of pose; per launch: the volume (and its gradient)."""
+    """Algorithmic HBM bytes per launch of each kernel: each unique input read once, each
+    output written once.  Per projection: Do*(Do/2+1)*8 B of image (written by the forward,
+    read by each backward kernel) and 4*(k*k+2) B of pose (read; the pose gradients are
+    written by the pose-gradient kernel); per launch: the volume (read by the gathers, the
+    volume gradient written by the scatter)."""
     img = wl.D * wl.H * 8
     k = wl.ndim
     pose = 4 * (k * k + 2)
     vol = wl.rec.nbytes
-    fwd = wl.B * (img + pose) + vol
-    bwd = wl.B * (img + 2 * pose) + 2 * vol
-    return fwd, bwd
+    return {"forward": wl.B * (img + pose) + vol,
+            "grad_pose": wl.B * (img + 2 * pose) + vol,
+            "grad_volume": wl.B * (img + pose) + vol}
 
 
 def kept_pixels(wl) -> int:
@@ -228,22 +232,28 @@ def run_ours(args, wl):
     gR = torch.empty_like(R)
     gS = torch.empty((1 if S is None else S.shape[0], wl.n_pose, 2), device=dev)
 
+    # The fused backward is issued as two C-ABI calls (pose gradients, then the volume
+    # gradient): the same outputs as one call, but each call is a single kernel, so CUDA
+    # events give every kernel's own duration.
     def step(ev=None):
         if ev is not None:
             ev[0].record(stream)
         tp.tp_project_3d_to_2d(V, R, S, Y, op, stream)
         if ev is not None:
             ev[1].record(stream)
-        tp.tp_project_backward(3, V, R, S, G, gV, gR, gS, op, stream)
+        tp.tp_project_backward(3, V, R, S, G, None, gR, gS, op, stream)
         if ev is not None:
             ev[2].record(stream)
+        tp.tp_project_backward(3, V, R, S, G, gV, None, None, op, stream)
+        if ev is not None:
+            ev[3].record(stream)
         if world > 1:
             dist.all_reduce(torch.view_as_real(gV))
 
     for _ in range(args.warmup):
         step()
     torch.cuda.synchronize()
-    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(args.steps)]
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(args.steps)]
     start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     uuid = None
     try:
@@ -269,8 +279,9 @@ def run_ours(args, wl):
         t = torch.tensor([ms], device=dev)
         dist.all_reduce(t, op=dist.ReduceOp.MAX)
         ms = float(t.item())
-    fwd_ms = statistics.mean(e[0].elapsed_time(e[1]) for e in evs)
-    bwd_ms = statistics.mean(e[1].elapsed_time(e[2]) for e in evs)
+    kms = {"forward": statistics.mean(e[0].elapsed_time(e[1]) for e in evs),
+           "grad_pose": statistics.mean(e[1].elapsed_time(e[2]) for e in evs),
+           "grad_volume": statistics.mean(e[2].elapsed_time(e[3]) for e in evs)}
     ms_step = ms / args.steps
     value = wl.B * world / (ms_step * 1e-3)
 
@@ -321,9 +332,8 @@ def run_ours(args, wl):
                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h}
 
     # roofline of the dominant kernel
-    fwd_b, bwd_b = hbm_bytes(wl)
-    dom = "backward" if bwd_ms >= fwd_ms else "forward"
-    dom_ms, dom_b = (bwd_ms, bwd_b) if dom == "backward" else (fwd_ms, fwd_b)
+    dom = max(kms, key=kms.get)
+    dom_ms = kms[dom]
     peaks = {}
     try:
         peaks = json.loads((ROOT / "MEASURED_PEAKS.json").read_text())
@@ -333,26 +343,29 @@ def run_ours(args, wl):
     peak_src = "measured"
     if peak is None:
         peak, peak_src = 6400.0, "fallback"
-    achieved = dom_b / (dom_ms * 1e-3) / 1e9
+    hbm = hbm_bytes(wl)
+    achieved = hbm[dom] / (dom_ms * 1e-3) / 1e9
     traffic = None
     try:
         tr = json.loads(TRAFFIC_FILE.read_text())
         ent = tr.get(wl.name, {}).get(dom)
         if ent and ent.get("kernel_hash") == kernel_hash():
-            traffic = ent["dram_bytes_per_launch"]
-    except (OSError, ValueError):
+            traffic = ent["dram_bytes_per_launch"] * (wl.B / ent["batch"])
+    except (OSError, ValueError, KeyError, ZeroDivisionError):
         pass
     taps = kept_pixels(wl) * wl.B * (64 if wl.interp else 8)
-    l1_bytes = {"forward": taps * 8, "backward": taps * 8 * 2}[dom]
+    onchip_bytes = {"forward": taps * 8, "grad_pose": taps * 8, "grad_volume": taps * 16}
     sm_mhz = (clocks or {}).get("sm_mhz") or peaks.get("sm_max_mhz", 2032.0)
     l1_peak = 148 * 128 * sm_mhz * 1e6 / 1e9
     roofline = {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                 "frac": achieved / peak, "traffic": traffic, "kernel": dom,
                 "peak_source": peak_src, "kernel_ms": dom_ms}
-    onchip = {"bound": "l1", "achieved": l1_bytes / (dom_ms * 1e-3) / 1e9,
-              "peak": l1_peak, "unit": "GB/s", "frac": l1_bytes / (dom_ms * 1e-3) / 1e9 / l1_peak,
-              "kernel": dom, "peak_source": "derived: 148 SM x 128 B/clk x median SM clock",
-              "bytes": "taps x 8 B (forward gather) / taps x 16 B (backward gather + scatter)"}
+    onchip = {k: {"achieved": onchip_bytes[k] / (kms[k] * 1e-3) / 1e9, "peak": l1_peak,
+                  "unit": "GB/s", "frac": onchip_bytes[k] / (kms[k] * 1e-3) / 1e9 / l1_peak}
+              for k in kms}
+    onchip["bound"] = "l1/smem data pipe"
+    onchip["peak_source"] = "derived: 148 SM x 128 B/clk x median SM clock"
+    onchip["bytes"] = "taps x 8 B (gathers) / taps x 16 B (scatter read-modify-write)"
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
@@ -368,8 +381,8 @@ def run_ours(args, wl):
             "data": "synthetic (seeded rfft of N(0,1) volume, uniform SO(3), CN(0,1) upstream grad)",
             "config": workload_config(wl, "inputs larger than L2 (1.09 GB upstream grad read and "
                                           "1.09 GB projections written per step); no flush"),
-            "gpu_launches": 2 * args.steps,
-            "kernel_ms": {"forward": fwd_ms, "backward": bwd_ms},
+            "gpu_launches": 3 * args.steps,
+            "kernel_ms": kms,
             "roofline": roofline, "roofline_onchip": onchip,
             "cpu_baseline": cpu, "e2e": e2e, "clocks": clocks,
         }
