@@ -173,7 +173,7 @@ __device__ __forceinline__ bool eval_fast(const Geom& g, const float2* __restric
 // ------------------------------------------------------------------ forward ----
 
 template <int NDIM, int INTERP, int WIN>
-__global__ void __launch_bounds__(kThreads) project_kernel(
+__global__ void __launch_bounds__(kThreads, 4) project_kernel(
     const float2* __restrict__ rec, const float* __restrict__ rot,
     const float* __restrict__ shift, float2* __restrict__ out, Geom g, long long n_items)
 {
@@ -790,15 +790,14 @@ constexpr int kTilePix = 16;                        // 4 x 4 pixels
 template <int INTERP>
 struct TileRec {
     static constexpr int NT = Taps<INTERP>::N;
-    // One record per pixel, stored contiguously (array of structs, odd stride) so that the
-    // lanes reading different fields of one pixel hit different banks:
-    // wzy[NT*NT] | wx[NT] | wt | gx gy | base fx fy fz (ints; base < 0 flags the
-    // per-tap path and holds ~base)
-    static constexpr int WZY = 0, WX = NT * NT, WT = NT * NT + NT, GX = WT + 1, GY = WT + 2;
-    static constexpr int BASE = WT + 3, FX = WT + 4, FY = WT + 5, FZ = WT + 6;
-    static constexpr int USED = WT + 7;
-    static constexpr int STRIDE = USED | 1;
-    static constexpr int WORDS = STRIDE * kTilePix > kBoxRows ? STRIDE * kTilePix : kBoxRows;
+    // One record per pixel, stored contiguously (array of structs): gx gy wt base (one
+    // 16-byte broadcast load) | wzy[NT*NT] | wx[NT] | fx fy fz.  base < 0 flags the per-tap
+    // path and holds ~base.
+    static constexpr int GX = 0, GY = 1, WT = 2, BASE = 3, WZY = 4, WX = 4 + NT * NT;
+    static constexpr int FX = WX + NT, FY = FX + 1, FZ = FX + 2;
+    static constexpr int USED = FZ + 1;
+    static constexpr int STRIDE = (USED + 3) / 4 * 4;  // 16-byte aligned records
+    static constexpr int WORDS = STRIDE * kTilePix;  // a multiple of 4: 16-byte aligned records
 };
 
 template <int INTERP, bool DATA, bool WTS>
@@ -823,7 +822,8 @@ __global__ void __launch_bounds__(kThreads) scatter_tile_kernel(
     float* recf = reinterpret_cast<float*>(reinterpret_cast<float2*>(sm_raw) + NWARP * (DATA ? kTileCap : 0)) +
                   NWARP * (WTS ? kTileCap : 0) + warp * TR::WORDS;
     int* reci = reinterpret_cast<int*>(recf);
-    int* rowoff = reci;  // reused after the pixel loop: global row offsets of the box rows
+    static_assert(TR::WORDS % 4 == 0 && (kTileCap * 4) % 16 == 0, "16-byte aligned records");
+
     __shared__ float Rs[9];
     __shared__ float2 sh;
 
@@ -952,10 +952,11 @@ __global__ void __launch_bounds__(kThreads) scatter_tile_kernel(
                     if (tap_lane) {
                         const float* rf = recf + j * TR::STRIDE;
                         const int* ri = reci + j * TR::STRIDE;
-                        const float2 gv = make_float2(rf[TR::GX], rf[TR::GY]);
-                        const float wtv = WTS ? rf[TR::WT] : 0.f;
+                        const float4 head = *reinterpret_cast<const float4*>(rf);
+                        const float2 gv = make_float2(head.x, head.y);
+                        const float wtv = head.z;
                         const float wxk = rf[TR::WX + tk];
-                        const int rb = ri[TR::BASE];
+                        const int rb = __float_as_int(head.w);
                         const int base = rb < 0 ? ~rb : rb;
                         if (rb >= 0) {
 #pragma unroll
@@ -1012,32 +1013,31 @@ __global__ void __launch_bounds__(kThreads) scatter_tile_kernel(
                     }
                     __syncwarp();
                 }
-                // ---- add the box to the volume (read and clear)
+                // ---- add the box to the volume (read and clear): the NX used columns of
+                // every box row; e / NX and r / NY by exact multiply-shift (e < 2^10, NX, NY <= 81)
                 if (boxed) {
-                    const int nrow = NY * NZ;
-                    for (int r = lane; r < nrow; r += 32) {
-                        const int zi = r / NY, yi = r - zi * NY;
+                    const int nused = NX * NY * NZ;
+                    const unsigned mx = (65536u + NX - 1) / NX, my = (65536u + NY - 1) / NY;
+                    for (int e = lane; e < nused; e += 32) {
+                        const int r = (int)(((unsigned)e * mx) >> 16);
+                        const int xi = e - r * NX;
+                        const int zi = (int)(((unsigned)r * my) >> 16);
+                        const int yi = r - zi * NY;
+                        const int ux = x0 + xi;
                         const int iy = full_index(y0 + yi, g.Dv, g.halfv, g.centered);
                         const int iz = full_index(z0 + zi, g.Dv, g.halfv, g.centered);
-                        rowoff[r] = (iy < 0 || iz < 0) ? -1 : (iz * g.Dv + iy) * g.Hv;
-                    }
-                    __syncwarp();
-                    const int nbox = nrow * kBoxPitch;
-                    for (int e = lane; e < nbox; e += 32) {
-                        const int r = (int)(((unsigned)e * 0xAAABu) >> 19);  // e / 12 for e < 2^15
-                        const int xi = e - r * kBoxPitch;
-                        const int ux = x0 + xi;
-                        const int ro = rowoff[r];
-                        const bool ok = xi < NX && ro >= 0 && ux >= 0 && ux <= g.halfv;
+                        const bool ok = iy >= 0 && iz >= 0 && ux >= 0 && ux <= g.halfv;
+                        const long long off = ((long long)iz * g.Dv + iy) * g.Hv + ux;
+                        const int be = r * kBoxPitch + xi;
                         if (DATA) {
-                            const float2 a = acc[e];
-                            if (ok && (a.x != 0.f || a.y != 0.f)) atomicAdd(G + ro + ux, a);
-                            acc[e] = make_float2(0.f, 0.f);
+                            const float2 a = acc[be];
+                            if (ok && (a.x != 0.f || a.y != 0.f)) atomicAdd(G + off, a);
+                            acc[be] = make_float2(0.f, 0.f);
                         }
                         if (WTS) {
-                            const float b = wacc[e];
-                            if (ok && b != 0.f) atomicAdd(Wt + ro + ux, b);
-                            wacc[e] = 0.f;
+                            const float b = wacc[be];
+                            if (ok && b != 0.f) atomicAdd(Wt + off, b);
+                            wacc[be] = 0.f;
                         }
                     }
                 }
