@@ -1047,6 +1047,59 @@ __global__ void __launch_bounds__(kThreads) scatter_tile_kernel(
     }
 }
 
+// Weight-volume part of the back-projection's backward: per kept pixel the real
+// interpolation v of the upstream weight-volume gradient (that is dL/d weight) and, for the
+// rotation gradient, weight * o q_b dv/dc_a summed per item (exact per-tap path).
+template <int NDIM, int INTERP, bool WANT_W, bool WANT_ROT>
+__global__ void __launch_bounds__(kThreads) weights_grad_kernel(
+    const float* __restrict__ gw, const float* __restrict__ weights, const float* __restrict__ rot,
+    float* __restrict__ gweights, float* __restrict__ grot, Geom g, int splits, long long n_work)
+{
+    __shared__ float red[kThreads / 32];
+    const int npix = (int)g.img_elems;
+    for (long long w = blockIdx.x; w < n_work; w += gridDim.x) {
+        const ItemRange ir = item_of(g, w, splits);
+        ItemParams<NDIM> ip;
+        load_item<NDIM>(g, rot, nullptr, ir.r, ir.p, ip);
+        const float* Wv = gw + (long long)ir.r * g.rec_elems;
+        const float* pw = weights ? weights + ir.item * g.img_elems : nullptr;
+        float* gwo = WANT_W ? gweights + ir.item * g.img_elems : nullptr;
+        float acc[2 * NDIM];
+#pragma unroll
+        for (int k = 0; k < 2 * NDIM; ++k) acc[k] = 0.f;
+        for (int pix = ir.part * kThreads + threadIdx.x; pix < npix; pix += splits * kThreads) {
+            int i, j;
+            split_pixel(pix, g.Ho, i, j);
+            const int ky = row_freq(i, g.Do, g.halfo, g.centered), kx = j;
+            if (kx * kx + ky * ky > g.rc2) {
+                if (WANT_W) gwo[pix] = 0.f;
+                continue;
+            }
+            PixelTaps<NDIM, INTERP, WANT_ROT> t;
+            t.init(g, ip.R, (float)kx, (float)ky);
+            float v, dv[3];
+            gather_real<NDIM, INTERP, WANT_ROT>(Wv, g, t, v, dv);
+            if (WANT_W) gwo[pix] = v;
+            if constexpr (WANT_ROT) {
+                const float wt = pw ? __ldg(pw + pix) : 1.f;
+#pragma unroll
+                for (int a = 0; a < NDIM; ++a) {
+                    acc[2 * a] = fmaf(wt * dv[a], (float)kx, acc[2 * a]);
+                    acc[2 * a + 1] = fmaf(wt * dv[a], (float)ky, acc[2 * a + 1]);
+                }
+            }
+        }
+        if constexpr (WANT_ROT) {
+            const long long ri = (long long)(g.rot_shared ? 0 : ir.r) * g.n_pose + ir.p;
+#pragma unroll
+            for (int k = 0; k < 2 * NDIM; ++k) {
+                const float s = block_sum(acc[k], red);
+                if (threadIdx.x == 0) atomicAdd(grot + ri * NDIM * NDIM + (k / 2) * NDIM + (k % 2), g.o * s);
+            }
+        }
+    }
+}
+
 // ------------------------------------------------------------------ launches ----
 
 struct LaunchShape {
@@ -1205,7 +1258,39 @@ void launch_backproject_t(const Geom& g, const float2* P, const float* weights, 
         launch_scatter_rows<NDIM, INTERP, false, true>(g, P, weights, rot, shift, VO, WO, sms, stream);
 }
 
+template <int NDIM, int INTERP>
+void launch_weights_grad_t(const Geom& g, const float* gw, const float* weights, const float* rot,
+                           float* gweights, float* grot, int sms, cudaStream_t stream)
+{
+    const LaunchShape s = launch_shape(g, sms);
+    if (gweights && grot)
+        weights_grad_kernel<NDIM, INTERP, true, true><<<s.grid, kThreads, 0, stream>>>(
+            gw, weights, rot, gweights, grot, g, s.splits, s.n_work);
+    else if (gweights)
+        weights_grad_kernel<NDIM, INTERP, true, false><<<s.grid, kThreads, 0, stream>>>(
+            gw, weights, rot, gweights, grot, g, s.splits, s.n_work);
+    else if (grot)
+        weights_grad_kernel<NDIM, INTERP, false, true><<<s.grid, kThreads, 0, stream>>>(
+            gw, weights, rot, gweights, grot, g, s.splits, s.n_work);
+}
+
 }  // namespace
+
+cudaError_t launch_weights_grad(int ndim, int interp, const Geom& g, const float* grad_wvol,
+                                const float* weights, const float* rot, float* grad_weights,
+                                float* grad_rot, int sms, cudaStream_t stream)
+{
+    if ((long long)g.n_rec * g.n_pose == 0 || (!grad_weights && !grad_rot)) return cudaSuccess;
+    if (ndim == 3 && interp == kCubic)
+        launch_weights_grad_t<3, kCubic>(g, grad_wvol, weights, rot, grad_weights, grad_rot, sms, stream);
+    else if (ndim == 3)
+        launch_weights_grad_t<3, kLinear>(g, grad_wvol, weights, rot, grad_weights, grad_rot, sms, stream);
+    else if (interp == kCubic)
+        launch_weights_grad_t<2, kCubic>(g, grad_wvol, weights, rot, grad_weights, grad_rot, sms, stream);
+    else
+        launch_weights_grad_t<2, kLinear>(g, grad_wvol, weights, rot, grad_weights, grad_rot, sms, stream);
+    return cudaGetLastError();
+}
 
 cudaError_t launch_project(int ndim, int interp, const Geom& g, const void* rec,
                            const float* rot, const float* shift, void* out, int sms,

@@ -22,4 +22,9 @@ cudaError_t launch_backproject(int ndim, int interp, const Geom& g, const void* 
                                const float* weights, const float* rot, const float* shift,
                                void* vol_out, float* wvol_out, int sms, cudaStream_t stream);
 
+// Weight-volume part of the back-projection's backward (see tp_backproject_backward).
+cudaError_t launch_weights_grad(int ndim, int interp, const Geom& g, const float* grad_wvol,
+                                const float* weights, const float* rot, float* grad_weights,
+                                float* grad_rot, int sms, cudaStream_t stream);
+
 }  // namespace tp

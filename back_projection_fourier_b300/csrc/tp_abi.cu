@@ -219,6 +219,61 @@ tp_status tp_project_backward(int ndim, const void* rec, int n_rec, int Dv, cons
     return e == cudaSuccess ? TP_OK : TP_ERR_CUDA;
 }
 
+tp_status tp_backproject_backward(int ndim, const void* proj, const float* weights, int n_rec,
+                                  int Do, const float* rot, int n_rot, int n_pose,
+                                  const float* shift, int n_sh, const void* grad_vol,
+                                  const float* grad_wvol, int Dv, void* grad_proj,
+                                  float* grad_weights, float* grad_rot, float* grad_shift,
+                                  const tp_opts* opts, void* stream)
+{
+    Opts o;
+    tp_status st = read_opts(opts, o);
+    if (st != TP_OK) return st;
+    st = check_common(ndim, n_rec, Dv, Do, n_rot, n_pose, shift, n_sh);
+    if (st != TP_OK) return st;
+    const long long n_items = (long long)n_rec * n_pose;
+    // the data part needs grad_vol (and proj for the pose gradients); NULL upstream = 0
+    const bool data_pose = grad_vol && (grad_rot || (grad_shift && shift));
+    const bool wts_part = grad_wvol && (grad_weights || grad_rot);
+    if (n_items > 0) {
+        if (!rot || (data_pose && !proj)) return TP_ERR_NULL;
+        if (!aligned(rot, 4) || (proj && !aligned(proj, 8)) || (grad_vol && !aligned(grad_vol, 8)) ||
+            (grad_wvol && !aligned(grad_wvol, 4)) || (weights && !aligned(weights, 4)) ||
+            (shift && !aligned(shift, 4)))
+            return TP_ERR_VALUE;
+    }
+    if ((grad_proj && !aligned(grad_proj, 8)) || (grad_weights && !aligned(grad_weights, 4)) ||
+        (grad_rot && !aligned(grad_rot, 4)) || (grad_shift && !aligned(grad_shift, 4)))
+        return TP_ERR_VALUE;
+    const tp::Geom g = make_geom(ndim, n_rec, Dv, n_rot, n_pose, shift, n_sh, Do, o);
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    const int k2 = ndim * ndim;
+    const size_t n_sh_rows = shift ? (size_t)n_sh : 1;
+    const size_t img_bytes = (size_t)g.img_elems * (size_t)n_items;
+    if (grad_rot && cudaMemsetAsync(grad_rot, 0, (size_t)n_rot * n_pose * k2 * 4, s) != cudaSuccess)
+        return TP_ERR_CUDA;
+    if (grad_shift && cudaMemsetAsync(grad_shift, 0, n_sh_rows * n_pose * 2 * 4, s) != cudaSuccess)
+        return TP_ERR_CUDA;
+    if (grad_proj && !grad_vol && cudaMemsetAsync(grad_proj, 0, img_bytes * 8, s) != cudaSuccess)
+        return TP_ERR_CUDA;
+    if (grad_weights && !grad_wvol && cudaMemsetAsync(grad_weights, 0, img_bytes * 4, s) != cudaSuccess)
+        return TP_ERR_CUDA;
+    if (n_items == 0) return TP_OK;
+    const int sms = sm_count();
+    cudaError_t e = cudaSuccess;
+    // Re<grad_vol, P^T proj> = Re<P grad_vol, proj>: the projection of grad_vol is the
+    // gradient for proj, and its pose gradients against proj are those of the insertion
+    if (grad_proj && grad_vol)
+        e = tp::launch_project(ndim, o.interp, g, grad_vol, rot, shift, grad_proj, sms, s);
+    if (e == cudaSuccess && data_pose)
+        e = tp::launch_backward(ndim, o.interp, g, grad_vol, rot, shift, proj, nullptr, grad_rot,
+                                grad_shift, sms, s);
+    if (e == cudaSuccess && wts_part)
+        e = tp::launch_weights_grad(ndim, o.interp, g, grad_wvol, weights, rot, grad_weights, grad_rot,
+                                    sms, s);
+    return e == cudaSuccess ? TP_OK : TP_ERR_CUDA;
+}
+
 const char* tp_status_string(tp_status status)
 {
     switch (status) {

@@ -310,6 +310,45 @@ __device__ __forceinline__ void gather(const float2* __restrict__ V, const Geom&
     }
 }
 
+// Real-volume variant of gather() for the weight volume: V_ext(t) = W[t] (t_x >= 0) or
+// W[-t] (t_x < 0) -- the Friedel mirror of a real array needs no conjugation.
+template <int NDIM, int INTERP, bool DERIV>
+__device__ __forceinline__ void gather_real(const float* __restrict__ Wv, const Geom& g,
+                                            const PixelTaps<NDIM, INTERP, DERIV>& t, float& v,
+                                            float* dv)
+{
+    constexpr int NT = Taps<INTERP>::N;
+    constexpr int NZ = NDIM == 3 ? NT : 1;
+    v = 0.f;
+    if constexpr (DERIV) dv[0] = dv[1] = dv[2] = 0.f;
+#pragma unroll
+    for (int a = 0; a < NZ; ++a) {
+#pragma unroll
+        for (int b = 0; b < NT; ++b) {
+            const int rd = t.row(g, a, b, false);
+            const int rm = t.row(g, a, b, true);
+            float rs = 0.f, rsd = 0.f;
+#pragma unroll
+            for (int k = 0; k < NT; ++k) {
+                const int tx = t.t0x + k;
+                const bool m = tx < 0;
+                const int ax = m ? -tx : tx;
+                const int r = m ? rm : rd;
+                const float val = (r >= 0 && ax <= g.halfv) ? __ldg(Wv + r + ax) : 0.f;
+                rs = fmaf(t.wx[k], val, rs);
+                if constexpr (DERIV) rsd = fmaf(t.dx[k], val, rsd);
+            }
+            const float wzy = t.wz[a] * t.wy[b];
+            v = fmaf(wzy, rs, v);
+            if constexpr (DERIV) {
+                dv[0] = fmaf(wzy, rsd, dv[0]);
+                dv[1] = fmaf(t.wz[a] * t.dy[b], rs, dv[1]);
+                if constexpr (NDIM == 3) dv[2] = fmaf(t.dz[a] * t.wy[b], rs, dv[2]);
+            }
+        }
+    }
+}
+
 // Transpose of gather(): G[t] += w(c - t) val for t_x >= 0 and G[-t] += conj(w(c - t) val)
 // for t_x < 0; W (real) receives w(c - t) wt on the same element, without conjugation.
 // Either destination may be null.

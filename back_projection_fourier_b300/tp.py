@@ -6,8 +6,8 @@ weights, C-contiguous) and derives the sizes from their shapes.  All the arithme
 in the CUDA kernels of libtp.so; there is no CPU or PyTorch fallback: importing this
 module fails when the library has not been built.
 
-The functional helpers at the end (``project``, ``backproject``, ``project_backward``)
-allocate the outputs with torch and call the ``tp_*`` functions.
+The functional helpers at the end (``project``, ``backproject``, ``project_backward``,
+``backproject_backward``) allocate the outputs with torch and call the ``tp_*`` functions.
 """
 from __future__ import annotations
 
@@ -50,10 +50,11 @@ def _load() -> ctypes.CDLL:
     L.tp_backproject_2d_to_3d.argtypes = [P, P, I, I, P, I, I, P, I, P, P, I, I, O, P]
     L.tp_backproject_2d_to_2d.argtypes = [P, P, I, I, P, I, I, P, I, P, P, I, I, O, P]
     L.tp_project_backward.argtypes = [I, P, I, I, P, I, I, P, I, P, I, P, P, P, O, P]
+    L.tp_backproject_backward.argtypes = [I, P, P, I, I, P, I, I, P, I, P, P, I, P, P, P, P, O, P]
     L.tp_status_string.argtypes = [I]
     L.tp_status_string.restype = ctypes.c_char_p
     for f in (L.tp_project_3d_to_2d, L.tp_project_2d_to_2d, L.tp_backproject_2d_to_3d,
-              L.tp_backproject_2d_to_2d, L.tp_project_backward):
+              L.tp_backproject_2d_to_2d, L.tp_project_backward, L.tp_backproject_backward):
         f.restype = I
     return L
 
@@ -178,6 +179,29 @@ def tp_project_backward(ndim, rec, rot, shift, grad_out, grad_rec, grad_rot, gra
                                    _stream(stream)), "tp_project_backward")
 
 
+def tp_backproject_backward(ndim, proj, weights, rot, shift, grad_vol, grad_wvol, grad_proj,
+                            grad_weights, grad_rot, grad_shift, opts=None, stream=None):
+    _need(proj, torch.complex64, "proj", 4)
+    _need(weights, torch.float32, "weights", 4)
+    _need(grad_vol, torch.complex64, "grad_vol", ndim + 1)
+    _need(grad_wvol, torch.float32, "grad_wvol", ndim + 1)
+    _need(grad_proj, torch.complex64, "grad_proj", 4)
+    _need(grad_weights, torch.float32, "grad_weights", 4)
+    _need(grad_rot, torch.float32, "grad_rot", 4)
+    _need(grad_shift, torch.float32, "grad_shift", 3)
+    n_rot, n_pose, n_sh = _rs(rot, shift, ndim)
+    ref = next(t for t in (proj, grad_proj, grad_weights, weights) if t is not None)
+    vref = grad_vol if grad_vol is not None else grad_wvol
+    if vref is None:
+        raise ValueError("grad_vol and grad_wvol are both None: the volume size is unknown")
+    _call(_LIB.tp_backproject_backward(int(ndim), _ptr(proj), _ptr(weights), ref.shape[0],
+                                       ref.shape[2], _ptr(rot), n_rot, n_pose, _ptr(shift), n_sh,
+                                       _ptr(grad_vol), _ptr(grad_wvol), vref.shape[1],
+                                       _ptr(grad_proj), _ptr(grad_weights), _ptr(grad_rot),
+                                       _ptr(grad_shift), _opts(opts), _stream(stream)),
+          "tp_backproject_backward")
+
+
 def tp_status_string(status: int) -> str:
     return _LIB.tp_status_string(int(status)).decode()
 
@@ -218,3 +242,20 @@ def project_backward(rec, rot, grad_out, shift=None, want_rec=True, want_rot=Tru
         if want_shift else None
     tp_project_backward(ndim, rec, rot, shift, grad_out, g_rec, g_rot, g_sh, opts, stream)
     return g_rec, g_rot, g_sh
+
+
+def backproject_backward(proj, rot, grad_vol, grad_wvol=None, shift=None, weights=None,
+                         want_proj=True, want_weights=True, want_rot=True, want_shift=True,
+                         opts=None, stream=None, ndim=3):
+    """Backward of the insertion: (grad_proj, grad_weights, grad_rot, grad_shift), each None
+    when not wanted (grad_weights also when weights is None)."""
+    g_proj = torch.empty_like(proj) if want_proj else None
+    g_w = torch.empty(proj.shape, dtype=torch.float32, device=proj.device) \
+        if want_weights and weights is not None else None
+    g_rot = torch.empty_like(rot) if want_rot else None
+    n_sh = shift.shape[0] if shift is not None else 1
+    g_sh = torch.empty((n_sh, rot.shape[1], 2), dtype=torch.float32, device=proj.device) \
+        if want_shift else None
+    tp_backproject_backward(ndim, proj, weights, rot, shift, grad_vol, grad_wvol, g_proj, g_w,
+                            g_rot, g_sh, opts, stream)
+    return g_proj, g_w, g_rot, g_sh

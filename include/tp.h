@@ -136,6 +136,32 @@ tp_status tp_project_backward(int ndim, const void* rec, int n_rec, int Dv, cons
                               const void* grad_out, int Do, void* grad_rec, float* grad_rot,
                               float* grad_shift, const tp_opts* opts, void* stream);
 
+/* Backward of tp_backproject_2d_to_3d (ndim = 3) or tp_backproject_2d_to_2d (ndim = 2): the
+ * gradients of the back-projection itself, for upstream gradients grad_vol (complex,
+ * reconstruction-shaped) of the data volume and grad_wvol (fp32, reconstruction-shaped) of
+ * the weight volume; either may be NULL (= 0).  Differentiation bullet ("all operations
+ * support gradients for inputs, rotations and shifts").  With vol = P^T(proj):
+ *   grad_proj    image-shaped complex = P(grad_vol), the forward projection of grad_vol
+ *                (overwritten; NULL = skip)
+ *   grad_weights image-shaped fp32 = the real interpolation of grad_wvol at every pixel
+ *                (Friedel mirror without conjugation, no phase; overwritten; NULL = skip)
+ *   grad_rot     [n_rot][n_pose][k][k]: d/dR of Re<P(grad_vol), proj> plus, with grad_wvol,
+ *                d/dR of sum weights * interp(grad_wvol) (overwritten; NULL = skip)
+ *   grad_shift   [n_sh][n_pose][2] (or [1][n_pose][2] without shift): d/ds of
+ *                Re<P(grad_vol), proj> (overwritten; NULL = skip)
+ * Layouts and shapes as in tp_backproject_2d_to_3d / tp_backproject_2d_to_2d (n_rec, Do
+ * describe proj, Dv the volumes).  proj is needed for grad_rot / grad_shift of the data
+ * part; weights (NULL = 1) for the weight part of grad_rot.  The caller owns every
+ * buffer; nothing is allocated.  Errors: TP_ERR_NULL when rot is NULL, or proj is NULL
+ * while grad_vol and grad_rot / grad_shift are given (n_rec * n_pose > 0); TP_ERR_SHAPE /
+ * TP_ERR_VALUE as for the forward; TP_ERR_CUDA when a launch fails. */
+tp_status tp_backproject_backward(int ndim, const void* proj, const float* weights, int n_rec,
+                                  int Do, const float* rot, int n_rot, int n_pose,
+                                  const float* shift, int n_sh, const void* grad_vol,
+                                  const float* grad_wvol, int Dv, void* grad_proj,
+                                  float* grad_weights, float* grad_rot, float* grad_shift,
+                                  const tp_opts* opts, void* stream);
+
 /* Static, NUL-terminated name of a status code (never NULL). */
 const char* tp_status_string(tp_status status);
 

@@ -9,6 +9,7 @@ from .oracle import (  # noqa: F401
     project_samples,
     backproject,
     project_backward,
+    backproject_backward,
     axis_weights,
     LINEAR,
     CUBIC,

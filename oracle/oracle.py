@@ -189,6 +189,49 @@ def project_backward(ndim, rec, rot, grad_out, shift=None, interp=CUBIC, layout=
     return g_rec, g_rot, g_sh
 
 
+def backproject_backward(ndim, proj, rot, grad_vol=None, grad_wvol=None, weights=None,
+                         shift=None, interp=CUBIC, layout=CENTERED, oversampling=1.0,
+                         cutoff=-1.0, nthreads=None):
+    """Gradients of the insertion (vol, wvol) = backproject(proj, weights, rot, shift) for the
+    upstream gradients grad_vol (complex) and grad_wvol (real); returns (grad_proj,
+    grad_weights, grad_rot, grad_shift).  torch-projectors summaries, Method section,
+    differentiation bullet: every operation is differentiable in its inputs, rotations and
+    shifts.
+
+    vol is real-linear in proj with the projection as its adjoint, so with
+    L = Re<grad_vol, vol> + <grad_wvol, wvol>:
+      grad_proj = P(grad_vol), and the data part's pose gradients are those of
+      Re<P(grad_vol), proj>, i.e. project_backward with rec = grad_vol, grad_out = proj;
+      wvol is linear in the weights with the same taps and no phase or conjugation, so
+      grad_weights = the projection of grad_wvol without shift (real), and the weight
+      part's rotation gradient is that of sum weights * P0(grad_wvol).
+    The composition is pinned against central differences of backproject() itself."""
+    proj = _c128(proj)
+    Do = proj.shape[2]
+    rot = _f64(rot)
+    kw = dict(interp=interp, layout=layout, oversampling=oversampling, cutoff=cutoff,
+              nthreads=nthreads)
+    n_sh = 1 if shift is None else np.asarray(shift).shape[0]
+    g_proj = np.zeros(proj.shape, np.complex128)
+    g_rot = np.zeros(rot.shape, np.float64)
+    g_sh = np.zeros((n_sh, rot.shape[1], 2), np.float64)
+    g_w = np.zeros(proj.shape, np.float64)
+    if grad_vol is not None:
+        g_proj = project(ndim, grad_vol, rot, shift, Do=Do, **kw)
+        _, gr, gs = project_backward(ndim, grad_vol, rot, proj, shift, want_rec=False, **kw)
+        g_rot += gr
+        if shift is not None:
+            g_sh += gs
+    if grad_wvol is not None:
+        gw = _c128(np.asarray(grad_wvol, np.float64))
+        g_w = project(ndim, gw, rot, None, Do=Do, **kw).real
+        w = np.ones(proj.shape) if weights is None else _f64(weights)
+        _, gr, _ = project_backward(ndim, gw, rot, w.astype(np.complex128), None, want_rec=False,
+                                    want_shift=False, **kw)
+        g_rot += gr
+    return g_proj, g_w, g_rot, g_sh
+
+
 def axis_weights(c: float, interp=CUBIC):
     """Taps, kernel weights and kernel derivatives of one axis at coordinate c."""
     t = np.zeros(4, np.int64)

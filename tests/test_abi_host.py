@@ -20,7 +20,8 @@ MIS = 0x10004           # 4-byte aligned, not 8-byte aligned
 def test_header_symbols_are_exported():
     names = tp.header_symbols()
     assert set(names) == {"tp_project_3d_to_2d", "tp_backproject_2d_to_3d", "tp_project_2d_to_2d",
-                          "tp_backproject_2d_to_2d", "tp_project_backward", "tp_status_string"}
+                          "tp_backproject_2d_to_2d", "tp_project_backward", "tp_backproject_backward",
+                          "tp_status_string"}
     for n in names:
         assert hasattr(L, n), n
     dyn = subprocess.run(["nm", "-D", "--defined-only", str(tp.LIB_PATH)], capture_output=True,
@@ -89,6 +90,35 @@ def test_backward_argument_errors():
     assert bw(3, None, 1, 8, FAKE, 1, 2, None, 1, FAKE, 8, None, FAKE, None, opts(), None) == 1
     assert bw(3, FAKE, 1, 8, FAKE, 1, 2, None, 1, FAKE, 6, FAKE, None, None, opts(cutoff=math.inf), None) == 3
     assert bw(2, FAKE, 2, 8, FAKE, 1, 2, FAKE, 3, FAKE, 8, FAKE, None, None, opts(), None) == 2
+
+
+def test_backproject_backward_argument_errors():
+    bb = L.tp_backproject_backward
+    # ndim, proj, weights, n_rec, Do, rot, n_rot, n_pose, shift, n_sh, grad_vol, grad_wvol, Dv,
+    # grad_proj, grad_weights, grad_rot, grad_shift, opts, stream
+    args = [3, FAKE, None, 1, 8, FAKE, 1, 2, None, 1, FAKE, None, 8, FAKE, None, FAKE, None, opts(), None]
+
+    def call(**kw):
+        a = list(args)
+        names = ["ndim", "proj", "weights", "n_rec", "Do", "rot", "n_rot", "n_pose", "shift", "n_sh",
+                 "grad_vol", "grad_wvol", "Dv", "grad_proj", "grad_weights", "grad_rot", "grad_shift",
+                 "opts"]
+        for k, v in kw.items():
+            a[names.index(k)] = v
+        return bb(*a)
+
+    assert call(ndim=1) == 3
+    assert call(rot=None) == 1
+    assert call(proj=None) == 1                      # data part of grad_rot needs proj
+    assert call(Dv=7) == 2
+    assert call(Do=4096) == 2
+    assert call(n_rec=2, n_rot=3) == 2
+    assert call(opts=opts(interp=5)) == 3
+    assert call(proj=MIS) == 3
+    assert call(grad_vol=MIS) == 3
+    assert call(grad_proj=MIS) == 3
+    assert call(grad_wvol=FAKE + 2) == 3
+    assert call(grad_weights=FAKE + 1) == 3
 
 
 def test_binding_rejects_bad_tensors():

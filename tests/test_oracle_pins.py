@@ -464,6 +464,68 @@ def test_gradient_of_volume_matches_directional_difference(orc):
         assert abs(fd - rdot(gV, E)) <= 1e-9 * abs(fd)
 
 
+@pytest.mark.parametrize("ndim,interp,layout,o,Dv,shifted,weighted,n_rec,n_rot",
+                         [(3, 1, 1, 1.0, 10, True, True, 1, 1), (3, 0, 0, 1.0, 10, True, True, 1, 1),
+                          (3, 1, 1, 1.0, 10, False, False, 2, 2),
+                          (2, 1, 1, 1.5, 14, True, True, 2, 1), (2, 0, 1, 1.0, 10, True, False, 2, 2)])
+def test_backproject_gradients_match_central_differences(orc, ndim, interp, layout, o, Dv, shifted,
+                                                         weighted, n_rec, n_rot):
+    """The insertion's backward (a composition of projections) against central differences
+    of the insertion itself: L = Re<Gv, vol> + <GW, wvol>, with (vol, wvol) from backproject()."""
+    Do, n_pose = 10, 3
+    Ho = Do // 2 + 1
+    seed = 40
+    while True:
+        rng = np.random.default_rng(seed)
+        R = random_rotations(rng, n_rot * n_pose, ndim).reshape(n_rot, n_pose, ndim, ndim)
+        if interp == 1 or _coords_clear_of_integers(R, Do, o):
+            break
+        seed += 1
+    Hv = Dv // 2 + 1
+    vshape = (n_rec, Dv, Dv, Hv) if ndim == 3 else (n_rec, Dv, Hv)
+    P = crandn(rng, (n_rec, n_pose, Do, Ho))
+    W = rng.uniform(0.2, 2.0, P.shape) if weighted else None
+    s = rng.uniform(-3, 3, (n_rot, n_pose, 2)) if shifted else None
+    Gv = crandn(rng, vshape)
+    GW = rng.standard_normal(vshape)
+    kw = dict(interp=interp, layout=layout, oversampling=o, cutoff=-1.0)
+
+    def L(P, W, R, s):
+        vol, wvol = orc.backproject(ndim, P, R, weights=W, shift=s, Dv=Dv, **kw)
+        return rdot(Gv, vol) + float(np.sum(GW * wvol))
+
+    gP, gW, gR, gs = orc.backproject_backward(ndim, P, R, Gv, GW, W, s, **kw)
+    h = 1e-6
+    for idx in np.ndindex(R.shape):
+        if ndim == 3 and idx[-1] == 2:
+            continue
+        Rp, Rm = R.copy(), R.copy()
+        Rp[idx] += h
+        Rm[idx] -= h
+        fd = (L(P, W, Rp, s) - L(P, W, Rm, s)) / (2 * h)
+        assert abs(fd - gR[idx]) <= 1e-6 * max(1.0, abs(fd)), (idx, fd, gR[idx])
+    if ndim == 3:
+        assert np.all(gR[..., 2] == 0)
+    if shifted:
+        for idx in np.ndindex(s.shape):
+            sp, sm = s.copy(), s.copy()
+            sp[idx] += h
+            sm[idx] -= h
+            fd = (L(P, W, R, sp) - L(P, W, R, sm)) / (2 * h)
+            assert abs(fd - gs[idx]) <= 1e-6 * max(1.0, abs(fd)), (idx, fd, gs[idx])
+    else:
+        assert np.all(gs == 0)
+    # L is linear in P and in W: the differences are exact up to rounding
+    Wb = W if weighted else np.ones(P.shape)
+    for _ in range(2):
+        E = crandn(rng, P.shape)
+        fd = (L(P + E, W, R, s) - L(P - E, W, R, s)) / 2
+        assert abs(fd - rdot(gP, E)) <= 1e-9 * max(1.0, abs(fd))
+        F = rng.standard_normal(P.shape)
+        fd = (L(P, Wb + F, R, s) - L(P, Wb - F, R, s)) / 2
+        assert abs(fd - float(np.sum(gW * F))) <= 1e-9 * max(1.0, abs(fd))
+
+
 def test_samples_match_full_projection(orc):
     rng = np.random.default_rng(31)
     D = 12

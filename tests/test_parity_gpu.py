@@ -116,6 +116,71 @@ def test_backproject_accumulate_and_skips(ndim):
     assert max_rel(host(vol), r_vol) <= TOL_BWD
 
 
+def _bp_grads(case, with_weights, seed):
+    ndim = case[0]
+    Gv, rot, shift, proj, w, kw, op = make_case(case, seed=seed)
+    rng = np.random.default_rng(seed + 100)
+    GW = rng.standard_normal(Gv.shape).astype(np.float32)
+    weights = w if with_weights else None
+    return ndim, Gv, GW, rot, shift, proj, weights, kw, op
+
+
+@pytest.mark.parametrize("case", CASES, ids=[str(c) for c in CASES])
+@pytest.mark.parametrize("with_weights", [True, False])
+def test_backproject_backward(case, with_weights):
+    """Gradients of the insertion for upstream gradients of both the data and weight volumes."""
+    ndim, Gv, GW, rot, shift, proj, weights, kw, op = _bp_grads(case, with_weights, 5)
+    gP, gW, gR, gs = tp.backproject_backward(dev(proj), dev(rot), dev(Gv), dev(GW), dev(shift),
+                                             dev(weights), want_shift=shift is not None, opts=op,
+                                             ndim=ndim)
+    rP, rW, rR, rs = oracle.backproject_backward(ndim, proj, rot, Gv, GW, weights, shift, **kw)
+    assert max_rel(host(gP), rP) <= TOL_FWD
+    if with_weights:
+        assert max_rel(host(gW), rW) <= TOL_FWD
+    assert max_rel(host(gR), rR) <= TOL_BWD
+    if ndim == 3:
+        assert np.all(host(gR)[..., 2] == 0)
+    if shift is not None:
+        assert max_rel(host(gs), rs) <= TOL_BWD
+
+
+@pytest.mark.parametrize("case", [CASES[0], CASES[3], CASES[6]], ids=str)
+def test_backproject_backward_partial(case):
+    """Either upstream gradient may be absent (= 0) and any output skipped."""
+    ndim, Gv, GW, rot, shift, proj, weights, kw, op = _bp_grads(case, True, 6)
+    # data volume only
+    rP, _, rR, rs = oracle.backproject_backward(ndim, proj, rot, Gv, None, weights, shift, **kw)
+    gP, gW, gR, gs = tp.backproject_backward(dev(proj), dev(rot), dev(Gv), None, dev(shift),
+                                             dev(weights), opts=op, ndim=ndim)
+    assert max_rel(host(gP), rP) <= TOL_FWD
+    assert np.all(host(gW) == 0)
+    assert max_rel(host(gR), rR) <= TOL_BWD
+    if shift is not None:
+        assert max_rel(host(gs), rs) <= TOL_BWD
+    else:
+        assert np.all(host(gs) == 0)
+    # weight volume only: no proj needed; the data gradients are zero
+    _, rW, rR, _ = oracle.backproject_backward(ndim, proj, rot, None, GW, weights, shift, **kw)
+    gP, gW, gR, gs = tp.backproject_backward(dev(proj), dev(rot), None, dev(GW), dev(shift),
+                                             dev(weights), opts=op, ndim=ndim)
+    assert np.all(host(gP) == 0) and np.all(host(gs) == 0)
+    assert max_rel(host(gW), rW) <= TOL_FWD
+    assert max_rel(host(gR), rR) <= TOL_BWD
+    # pose gradients only, then the image gradients only (proj not needed)
+    _, rW, rR, rs = oracle.backproject_backward(ndim, proj, rot, Gv, GW, weights, shift, **kw)
+    _, _, gR, gs = tp.backproject_backward(dev(proj), dev(rot), dev(Gv), dev(GW), dev(shift),
+                                           dev(weights), want_proj=False, want_weights=False,
+                                           opts=op, ndim=ndim)
+    assert max_rel(host(gR), rR) <= TOL_BWD
+    gP = torch.empty(proj.shape, dtype=torch.complex64, device="cuda")
+    gW = torch.empty(proj.shape, dtype=torch.float32, device="cuda")
+    tp.tp_backproject_backward(ndim, None, None, dev(rot), dev(shift), dev(Gv), dev(GW), gP, gW,
+                               None, None, op)
+    rP = oracle.project(ndim, Gv, rot, shift, Do=proj.shape[2], **kw)
+    assert max_rel(host(gP), rP) <= TOL_FWD
+    assert max_rel(host(gW), rW) <= TOL_FWD
+
+
 def test_empty_batches():
     vol = torch.ones((1, 8, 8, 5), dtype=torch.complex64, device="cuda")
     rot = torch.zeros((1, 0, 3, 3), device="cuda")
@@ -127,6 +192,8 @@ def test_empty_batches():
     assert torch.all(vol == 0) and torch.all(w == 0)
     g_rot = torch.full((1, 0, 3, 3), 7.0, device="cuda")
     tp.tp_project_backward(3, vol, rot, None, out, vol, g_rot, None)
+    gw = torch.empty((1, 0, 8, 5), device="cuda")
+    tp.tp_backproject_backward(3, out, gw, rot, None, vol, w, out, gw, g_rot, None)
     torch.cuda.synchronize()
 
 
