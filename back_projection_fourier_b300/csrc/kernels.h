@@ -27,4 +27,11 @@ cudaError_t launch_weights_grad(int ndim, int interp, const Geom& g, const float
                                 const float* weights, const float* rot, float* grad_weights,
                                 float* grad_rot, int sms, cudaStream_t stream);
 
+// Real-space zero padding by an integer factor with the centre moved to index 0, and its
+// adjoint (pad.cu).  vol / out are [n][D]^ndim and [n][factor*D]^ndim fp32.
+cudaError_t launch_pad(int ndim, const float* vol, int n, int D, int factor, float* out, int sms,
+                       cudaStream_t stream);
+cudaError_t launch_crop(int ndim, const float* padded, int n, int D, int factor, float* out,
+                        int sms, cudaStream_t stream);
+
 }  // namespace tp

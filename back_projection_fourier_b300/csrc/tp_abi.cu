@@ -274,6 +274,44 @@ tp_status tp_backproject_backward(int ndim, const void* proj, const float* weigh
     return e == cudaSuccess ? TP_OK : TP_ERR_CUDA;
 }
 
+namespace {
+
+constexpr int kMaxPadFactor = 8;
+
+tp_status check_pad(int ndim, const void* a, const void* b, int n_rec, int D, int factor)
+{
+    if (ndim != 2 && ndim != 3) return TP_ERR_VALUE;
+    if (factor < 1 || factor > kMaxPadFactor) return TP_ERR_VALUE;
+    if (n_rec < 0 || D < 2 || (D % 2) != 0) return TP_ERR_SHAPE;
+    if (!box_ok((long long)factor * D > INT_MAX ? -1 : factor * D, ndim)) return TP_ERR_SHAPE;
+    if (n_rec == 0) return TP_OK;
+    if (!a || !b) return TP_ERR_NULL;
+    if (!aligned(a, 4) || !aligned(b, 4)) return TP_ERR_VALUE;
+    return TP_OK;
+}
+
+}  // namespace
+
+tp_status tp_pad_volume(int ndim, const float* vol, int n_rec, int D, int factor, float* out,
+                        void* stream)
+{
+    const tp_status st = check_pad(ndim, vol, out, n_rec, D, factor);
+    if (st != TP_OK || n_rec == 0) return st;
+    const cudaError_t e = tp::launch_pad(ndim, vol, n_rec, D, factor, out, sm_count(),
+                                         static_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? TP_OK : TP_ERR_CUDA;
+}
+
+tp_status tp_crop_volume(int ndim, const float* padded, int n_rec, int D, int factor, float* out,
+                         void* stream)
+{
+    const tp_status st = check_pad(ndim, padded, out, n_rec, D, factor);
+    if (st != TP_OK || n_rec == 0) return st;
+    const cudaError_t e = tp::launch_crop(ndim, padded, n_rec, D, factor, out, sm_count(),
+                                          static_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? TP_OK : TP_ERR_CUDA;
+}
+
 const char* tp_status_string(tp_status status)
 {
     switch (status) {

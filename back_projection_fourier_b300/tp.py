@@ -7,7 +7,8 @@ in the CUDA kernels of libtp.so; there is no CPU or PyTorch fallback: importing 
 module fails when the library has not been built.
 
 The functional helpers at the end (``project``, ``backproject``, ``project_backward``,
-``backproject_backward``) allocate the outputs with torch and call the ``tp_*`` functions.
+``backproject_backward``, ``pad_volume``, ``crop_volume``) allocate the outputs with torch
+and call the ``tp_*`` functions.
 """
 from __future__ import annotations
 
@@ -51,10 +52,13 @@ def _load() -> ctypes.CDLL:
     L.tp_backproject_2d_to_2d.argtypes = [P, P, I, I, P, I, I, P, I, P, P, I, I, O, P]
     L.tp_project_backward.argtypes = [I, P, I, I, P, I, I, P, I, P, I, P, P, P, O, P]
     L.tp_backproject_backward.argtypes = [I, P, P, I, I, P, I, I, P, I, P, P, I, P, P, P, P, O, P]
+    L.tp_pad_volume.argtypes = [I, P, I, I, I, P, P]
+    L.tp_crop_volume.argtypes = [I, P, I, I, I, P, P]
     L.tp_status_string.argtypes = [I]
     L.tp_status_string.restype = ctypes.c_char_p
     for f in (L.tp_project_3d_to_2d, L.tp_project_2d_to_2d, L.tp_backproject_2d_to_3d,
-              L.tp_backproject_2d_to_2d, L.tp_project_backward, L.tp_backproject_backward):
+              L.tp_backproject_2d_to_2d, L.tp_project_backward, L.tp_backproject_backward,
+              L.tp_pad_volume, L.tp_crop_volume):
         f.restype = I
     return L
 
@@ -202,6 +206,20 @@ def tp_backproject_backward(ndim, proj, weights, rot, shift, grad_vol, grad_wvol
           "tp_backproject_backward")
 
 
+def tp_pad_volume(ndim, vol, factor, out, stream=None):
+    _need(vol, torch.float32, "vol", ndim + 1)
+    _need(out, torch.float32, "out", ndim + 1)
+    _call(_LIB.tp_pad_volume(int(ndim), _ptr(vol), vol.shape[0], vol.shape[-1], int(factor),
+                             _ptr(out), _stream(stream)), "tp_pad_volume")
+
+
+def tp_crop_volume(ndim, padded, factor, out, stream=None):
+    _need(padded, torch.float32, "padded", ndim + 1)
+    _need(out, torch.float32, "out", ndim + 1)
+    _call(_LIB.tp_crop_volume(int(ndim), _ptr(padded), out.shape[0], out.shape[-1], int(factor),
+                              _ptr(out), _stream(stream)), "tp_crop_volume")
+
+
 def tp_status_string(status: int) -> str:
     return _LIB.tp_status_string(int(status)).decode()
 
@@ -259,3 +277,19 @@ def backproject_backward(proj, rot, grad_vol, grad_wvol=None, shift=None, weight
     tp_backproject_backward(ndim, proj, weights, rot, shift, grad_vol, grad_wvol, g_proj, g_w,
                             g_rot, g_sh, opts, stream)
     return g_proj, g_w, g_rot, g_sh
+
+
+def pad_volume(vol, factor, ndim=3, stream=None):
+    """Zero-pad [n][D]^ndim real data by `factor`, centre moved to index 0."""
+    P = int(factor) * vol.shape[-1]
+    out = torch.empty((vol.shape[0],) + (P,) * ndim, dtype=torch.float32, device=vol.device)
+    tp_pad_volume(ndim, vol, factor, out, stream)
+    return out
+
+
+def crop_volume(padded, D, factor, ndim=3, stream=None):
+    """Adjoint of pad_volume: the [n][D]^ndim box back out of the padded array."""
+    out = torch.empty((padded.shape[0],) + (int(D),) * ndim, dtype=torch.float32,
+                      device=padded.device)
+    tp_crop_volume(ndim, padded, factor, out, stream)
+    return out

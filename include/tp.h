@@ -162,6 +162,31 @@ tp_status tp_backproject_backward(int ndim, const void* proj, const float* weigh
                                   float* grad_weights, float* grad_rot, float* grad_shift,
                                   const tp_opts* opts, void* stream);
 
+/* Real-space zero padding for on-the-fly oversampling.  Dutch page, problem statement
+ * (oversampling is zero-filling in the spatial domain and needs Fourier transforms on
+ * every pass); Spanish page, results, comparison bullet; French page, interpolation
+ * comparison (linear with on-the-fly padding and extra FFTs against cubic without).
+ *   vol  [n_rec][D][D][D] (ndim = 3) or [n_rec][D][D] (ndim = 2) fp32 real-space data
+ *        whose centre is at index D/2 on every axis (read)
+ *   out  [n_rec][P][P][P] or [n_rec][P][P] fp32, P = factor * D (overwritten): the volume
+ *        centred in the P box, zeros elsewhere, with the centre moved to index 0 (the
+ *        ifftshift of the padded box), so that a real-to-complex FFT of out is the
+ *        oversampled half spectrum in FFTW order; sampling it at c = factor * R q
+ *        (tp_opts.oversampling = factor, layout TP_LAYOUT_FFTW) gives the projection of
+ *        the volume at box D.  factor = 1 is the plain ifftshift.
+ * D even >= 2, 1 <= factor <= 8, P within the box limit of the projection (1024 in 3D,
+ * 32768 in 2D).  Errors: TP_ERR_VALUE for ndim / factor / misaligned pointers,
+ * TP_ERR_SHAPE for sizes, TP_ERR_NULL for a NULL pointer with n_rec > 0. */
+tp_status tp_pad_volume(int ndim, const float* vol, int n_rec, int D, int factor, float* out,
+                        void* stream);
+
+/* Adjoint of tp_pad_volume (and its left inverse): out [n_rec][D]^ndim = the entries of
+ * padded [n_rec][P]^ndim that tp_pad_volume filled from the volume.  It is the gradient
+ * of the padding for an upstream gradient `padded`.  Arguments and errors as in
+ * tp_pad_volume. */
+tp_status tp_crop_volume(int ndim, const float* padded, int n_rec, int D, int factor, float* out,
+                         void* stream);
+
 /* Static, NUL-terminated name of a status code (never NULL). */
 const char* tp_status_string(tp_status status);
 

@@ -10,6 +10,11 @@ from .oracle import (  # noqa: F401
     backproject,
     project_backward,
     backproject_backward,
+    pad_volume,
+    crop_volume,
+    oversampled_spectrum,
+    project_real,
+    project_real_backward,
     axis_weights,
     LINEAR,
     CUBIC,

@@ -232,6 +232,68 @@ def backproject_backward(ndim, proj, rot, grad_vol=None, grad_wvol=None, weights
     return g_proj, g_w, g_rot, g_sh
 
 
+def pad_volume(vol, factor: int):
+    """Real-space zero padding for on-the-fly oversampling (Dutch page, problem statement:
+    oversampling is zero-filling in the spatial domain; French page, interpolation
+    comparison).  vol is [n][D]^k real with its centre at index D/2; the result is the
+    [n][factor*D]^k box holding vol centred, zeros elsewhere, ifftshifted so that the centre
+    sits at index 0 (np.pad, then np.fft.ifftshift over the spatial axes)."""
+    vol = np.asarray(vol, np.float64)
+    D = vol.shape[-1]
+    k = vol.ndim - 1
+    m = (factor - 1) * D // 2
+    padded = np.pad(vol, [(0, 0)] + [(m, m)] * k)
+    return np.fft.ifftshift(padded, axes=tuple(range(1, k + 1)))
+
+
+def crop_volume(padded, D: int):
+    """Adjoint and left inverse of pad_volume: undo the shift, cut the centred D box out."""
+    padded = np.asarray(padded, np.float64)
+    k = padded.ndim - 1
+    P = padded.shape[-1]
+    m = (P - D) // 2
+    c = np.fft.fftshift(padded, axes=tuple(range(1, k + 1)))
+    return c[(slice(None),) + (slice(m, m + D),) * k]
+
+
+def oversampled_spectrum(vol, factor: int):
+    """Half spectrum (FFTW order) of the padded volume: numpy's rfftn of pad_volume."""
+    k = np.asarray(vol).ndim - 1
+    return np.fft.rfftn(pad_volume(vol, factor), axes=tuple(range(1, k + 1)))
+
+
+def project_real(ndim, vol, rot, shift=None, factor=1, interp=CUBIC, cutoff=-1.0, nthreads=None):
+    """On-the-fly pipeline from a real-space volume of box D to its projections at box D:
+    pad by `factor`, FFT, then sample the oversampled spectrum at c = factor * R q (FFTW
+    layout).  factor = 1 with cubic weights and factor = 2 with linear weights are the two
+    alternatives the pages compare."""
+    D = np.asarray(vol).shape[-1]
+    spec = oversampled_spectrum(vol, factor)
+    return project(ndim, spec, rot, shift, Do=D, interp=interp, layout=FFTW,
+                   oversampling=float(factor), cutoff=cutoff, nthreads=nthreads)
+
+
+def project_real_backward(ndim, vol, rot, grad_out, shift=None, factor=1, interp=CUBIC,
+                          cutoff=-1.0, nthreads=None):
+    """Gradients of project_real for the upstream grad_out (PyTorch's complex convention):
+    (grad_vol real, grad_rot, grad_shift).  With g the gradient of the half spectrum
+    X_k = sum_n x_n exp(-2 pi i k.n / P), dL/dx_n = Re sum_k conj(g_k) exp(-2 pi i k.n / P)
+    = Re(P^k * ifftn(g placed in the full spectrum, zeros in the other half))_n; the
+    volume's gradient is then the adjoint of the padding (crop_volume)."""
+    vol = np.asarray(vol, np.float64)
+    D = vol.shape[-1]
+    spec = oversampled_spectrum(vol, factor)
+    g_spec, g_rot, g_sh = project_backward(ndim, spec, rot, grad_out, shift, interp=interp,
+                                           layout=FFTW, oversampling=float(factor),
+                                           cutoff=cutoff, nthreads=nthreads)
+    P = factor * D
+    axes = tuple(range(1, ndim + 1))
+    full = np.zeros(vol.shape[:1] + (P,) * ndim, np.complex128)
+    full[..., : P // 2 + 1] = g_spec
+    g_x = np.real(np.fft.ifftn(full, axes=axes)) * float(P) ** ndim
+    return crop_volume(g_x, D), g_rot, g_sh
+
+
 def axis_weights(c: float, interp=CUBIC):
     """Taps, kernel weights and kernel derivatives of one axis at coordinate c."""
     t = np.zeros(4, np.int64)

@@ -21,7 +21,7 @@ def test_header_symbols_are_exported():
     names = tp.header_symbols()
     assert set(names) == {"tp_project_3d_to_2d", "tp_backproject_2d_to_3d", "tp_project_2d_to_2d",
                           "tp_backproject_2d_to_2d", "tp_project_backward", "tp_backproject_backward",
-                          "tp_status_string"}
+                          "tp_pad_volume", "tp_crop_volume", "tp_status_string"}
     for n in names:
         assert hasattr(L, n), n
     dyn = subprocess.run(["nm", "-D", "--defined-only", str(tp.LIB_PATH)], capture_output=True,
@@ -119,6 +119,21 @@ def test_backproject_backward_argument_errors():
     assert call(grad_proj=MIS) == 3
     assert call(grad_wvol=FAKE + 2) == 3
     assert call(grad_weights=FAKE + 1) == 3
+
+
+@pytest.mark.parametrize("fn", ["tp_pad_volume", "tp_crop_volume"])
+def test_pad_argument_errors(fn):
+    f = getattr(L, fn)
+    assert f(4, FAKE, 1, 8, 2, FAKE, None) == 3
+    assert f(3, FAKE, 1, 8, 0, FAKE, None) == 3
+    assert f(3, FAKE, 1, 8, 9, FAKE, None) == 3
+    assert f(3, FAKE, 1, 7, 2, FAKE, None) == 2
+    assert f(3, FAKE, -1, 8, 2, FAKE, None) == 2
+    assert f(3, FAKE, 1, 768, 2, FAKE, None) == 2     # padded box beyond the 3D limit
+    assert f(3, None, 1, 8, 2, FAKE, None) == 1
+    assert f(3, FAKE, 1, 8, 2, None, None) == 1
+    assert f(3, FAKE + 2, 1, 8, 2, FAKE, None) == 3
+    assert f(3, None, 0, 8, 2, None, None) == 0
 
 
 def test_binding_rejects_bad_tensors():
