@@ -137,6 +137,26 @@ __device__ __forceinline__ float block_sum(float v, float* red)
     return s;
 }
 
+// Work split of one item's kept pixels over `splits` CTAs: chunks of whole CTA rounds.
+__device__ __forceinline__ int kept_chunk(int nkept, int splits)
+{
+    return ((nkept + splits - 1) / splits + kThreads - 1) / kThreads * kThreads;
+}
+
+// Image row holding kept pixel n0: the largest row r < Do with rowstart[r] <= n0.
+__device__ __forceinline__ int row_of_kept(const int* rowstart, int Do, int n0)
+{
+    int lo = 0, hi = Do - 1;
+    while (lo < hi) {
+        const int mid = (lo + hi + 1) >> 1;
+        if (rowstart[mid] <= n0)
+            lo = mid;
+        else
+            hi = mid - 1;
+    }
+    return lo;
+}
+
 // ------------------------------------------------------- per-pixel evaluation ----
 
 // Exact per-tap evaluation in the original frame (any pixel).
@@ -175,7 +195,7 @@ __device__ __forceinline__ bool eval_fast(const Geom& g, const float2* __restric
 template <int NDIM, int INTERP, int WIN>
 __global__ void __launch_bounds__(kThreads, 4) project_kernel(
     const float2* __restrict__ rec, const float* __restrict__ rot,
-    const float* __restrict__ shift, float2* __restrict__ out, Geom g, long long n_items)
+    const float* __restrict__ shift, float2* __restrict__ out, Geom g, int splits, long long n_work)
 {
     extern __shared__ int smem[];
     int* rowstart = smem;                    // [Do + 1]
@@ -188,15 +208,17 @@ __global__ void __launch_bounds__(kThreads, 4) project_kernel(
     const Queue q{qslots, &qcount};
     const int nkept = rowstart[g.Do];
     const int npix = (int)g.img_elems;
+    const int chunk = kept_chunk(nkept, splits);
 
-    for (long long item = blockIdx.x; item < n_items; item += gridDim.x) {
-        const ItemRange ir = item_of(g, item, 1);
+    // work unit = (item, part): part takes one chunk of the item's kept pixels
+    for (long long w = blockIdx.x; w < n_work; w += gridDim.x) {
+        const ItemRange ir = item_of(g, w, splits);
         ItemParams<NDIM> ip;
         load_item<NDIM>(g, rot, shift, ir.r, ir.p, ip);
         const float2* V = rec + (long long)ir.r * g.rec_elems;
         float2* y = out + ir.item * g.img_elems;
         // pixels beyond the cutoff are zero
-        for (int p = threadIdx.x; p < npix; p += kThreads) {
+        for (int p = ir.part * kThreads + threadIdx.x; p < npix; p += splits * kThreads) {
             int i, j;
             split_pixel(p, g.Ho, i, j);
             if (j >= rowstart[i + 1] - rowstart[i]) y[p] = make_float2(0.f, 0.f);
@@ -207,12 +229,13 @@ __global__ void __launch_bounds__(kThreads, 4) project_kernel(
                 val = cmul(val, shift_phase((float)kx, (float)ky, ip.sx, ip.sy, g.Do_f, g.inv_Do));
             y[row * g.Ho + kx] = val;
         };
-        int row = 0;
-        for (int base = 0; base < nkept; base += kThreads) {
+        const int b0 = ir.part * chunk, b1 = min(nkept, b0 + chunk);
+        int row = b0 < nkept ? row_of_kept(rowstart, g.Do, b0) : 0;
+        for (int base = b0; base < b1; base += kThreads) {
             const int n = base + threadIdx.x;
             bool slow = false;
             int kx = 0;
-            if (n < nkept) {
+            if (n < b1) {
                 while (rowstart[row + 1] <= n) ++row;
                 kx = n - rowstart[row];
                 const int ky = row_freq(row, g.Do, g.halfo, g.centered);
@@ -303,7 +326,7 @@ template <int NDIM, int INTERP, int WIN>
 __global__ void __launch_bounds__(kThreads) grad_pose_kernel(
     const float2* __restrict__ rec, const float* __restrict__ rot,
     const float* __restrict__ shift, const float2* __restrict__ gout,
-    float* __restrict__ grot, float* __restrict__ gsh, Geom g, long long n_items)
+    float* __restrict__ grot, float* __restrict__ gsh, Geom g, int splits, long long n_work)
 {
     constexpr int NG = NDIM * 2 + 2;
     extern __shared__ int smem[];
@@ -317,9 +340,11 @@ __global__ void __launch_bounds__(kThreads) grad_pose_kernel(
     __syncthreads();
     const Queue q{qslots, &qcount};
     const int nkept = rowstart[g.Do];
+    const int chunk = kept_chunk(nkept, splits);
 
-    for (long long item = blockIdx.x; item < n_items; item += gridDim.x) {
-        const ItemRange ir = item_of(g, item, 1);
+    // work unit = (item, part): part sums one chunk of the item's kept pixels
+    for (long long w = blockIdx.x; w < n_work; w += gridDim.x) {
+        const ItemRange ir = item_of(g, w, splits);
         ItemParams<NDIM> ip;
         load_item<NDIM>(g, rot, shift, ir.r, ir.p, ip);
         const float2* V = rec + (long long)ir.r * g.rec_elems;
@@ -334,12 +359,13 @@ __global__ void __launch_bounds__(kThreads) grad_pose_kernel(
                 gp = cmul_conj(gp, shift_phase((float)kx, (float)ky, ip.sx, ip.sy, g.Do_f, g.inv_Do));
             accumulate_grad<NDIM>(acc, gp, v, dv, kx, ky);
         };
-        int row = 0;
-        for (int base = 0; base < nkept; base += kThreads) {
+        const int b0 = ir.part * chunk, b1 = min(nkept, b0 + chunk);
+        int row = b0 < nkept ? row_of_kept(rowstart, g.Do, b0) : 0;
+        for (int base = b0; base < b1; base += kThreads) {
             const int n = base + threadIdx.x;
             bool slow = false;
             int kx = 0;
-            if (n < nkept) {
+            if (n < b1) {
                 while (rowstart[row + 1] <= n) ++row;
                 kx = n - rowstart[row];
                 const int ky = row_freq(row, g.Do, g.halfo, g.centered);
@@ -804,7 +830,7 @@ template <int INTERP, bool DATA, bool WTS>
 __global__ void __launch_bounds__(kThreads) scatter_tile_kernel(
     const float2* __restrict__ proj, const float* __restrict__ wts,
     const float* __restrict__ rot, const float* __restrict__ shift,
-    float2* __restrict__ vout, float* __restrict__ wout, Geom g, long long n_items)
+    float2* __restrict__ vout, float* __restrict__ wout, Geom g, int splits, long long n_work)
 {
     using TR = TileRec<INTERP>;
     constexpr int NT = Taps<INTERP>::N;
@@ -844,8 +870,9 @@ __global__ void __launch_bounds__(kThreads) scatter_tile_kernel(
     const int tiles_x = (g.Ho + 3) / 4, tiles_y = (g.Do + 3) / 4;
     const int ntiles = tiles_x * tiles_y;
 
-    for (long long item = blockIdx.x; item < n_items; item += gridDim.x) {
-        const ItemRange ir = item_of(g, item, 1);
+    // work unit = (item, part): part takes every splits-th round of NWARP tiles
+    for (long long w = blockIdx.x; w < n_work; w += gridDim.x) {
+        const ItemRange ir = item_of(g, w, splits);
         __syncthreads();
         if (threadIdx.x < 9) {
             const long long ri = (long long)(g.rot_shared ? 0 : ir.r) * g.n_pose + ir.p;
@@ -864,7 +891,7 @@ __global__ void __launch_bounds__(kThreads) scatter_tile_kernel(
         float2* G = DATA ? vout + (long long)ir.r * g.rec_elems : nullptr;
         float* Wt = WTS ? wout + (long long)ir.r * g.rec_elems : nullptr;
 
-        for (int tile = warp; tile < ntiles; tile += NWARP) {
+        for (int tile = ir.part * NWARP + warp; tile < ntiles; tile += splits * NWARP) {
             const int ti = tile / tiles_x, tj = tile - ti * tiles_x;
             // ---- per-pixel set-up: lane l < 16 owns pixel (row 4 ti + l / 4, kx 4 tj + l % 4)
             const int prow = 4 * ti + (lane >> 2), pkx = 4 * tj + (lane & 3);
@@ -1125,18 +1152,33 @@ LaunchShape launch_shape(const Geom& g, int sms)
     return s;
 }
 
-// Table kernels: one CTA per item at a time, grid = a few waves of resident CTAs.
+// Splits of one item over CTAs so that a small batch still fills `target` CTAs: at most
+// `max_parts` (the item's units of work), at least 1.
+long long item_splits(long long n_items, long long target, long long max_parts)
+{
+    long long splits = 1;
+    if (n_items > 0 && n_items < target) splits = (target + n_items - 1) / n_items;
+    if (splits > max_parts) splits = max_parts;
+    return splits < 1 ? 1 : splits;
+}
+
+// Table kernels: one CTA per (item, part) at a time, grid = a few waves of resident CTAs.
 struct TableShape {
     unsigned grid;
     size_t smem;
+    int splits;
+    long long n_work;
 };
 
-TableShape table_shape(const Geom& g, int sms)
+TableShape table_shape(const Geom& g, int sms, int ctas_per_sm)
 {
     const long long n_items = (long long)g.n_rec * g.n_pose;
-    const long long cap = 16LL * sms;  // persistent-style: the table is built once per CTA
+    const long long max_parts = (g.img_elems + kThreads - 1) / kThreads;
     TableShape t;
-    t.grid = (unsigned)(n_items < cap ? n_items : cap);
+    t.splits = (int)item_splits(n_items, (long long)ctas_per_sm * sms, max_parts);
+    t.n_work = n_items * t.splits;
+    const long long cap = 16LL * sms;  // persistent-style: the table is built once per CTA
+    t.grid = (unsigned)(t.n_work < cap ? t.n_work : cap);
     t.smem = (size_t)(g.Do + 1 + kQueue) * sizeof(int);
     return t;
 }
@@ -1151,9 +1193,9 @@ template <int NDIM, int INTERP, int WIN>
 void launch_project_table(const Geom& g, const float2* R, const float* rot, const float* shift,
                           float2* Y, int sms, cudaStream_t stream)
 {
-    const TableShape t = table_shape(g, sms);
+    const TableShape t = table_shape(g, sms, 4);
     project_kernel<NDIM, INTERP, WIN><<<t.grid, kThreads, t.smem, stream>>>(
-        R, rot, shift, Y, g, (long long)g.n_rec * g.n_pose);
+        R, rot, shift, Y, g, t.splits, t.n_work);
 }
 
 template <int NDIM, int INTERP>
@@ -1178,9 +1220,9 @@ template <int NDIM, int INTERP, int WIN>
 void launch_grad_table(const Geom& g, const float2* R, const float* rot, const float* shift,
                        const float2* G, float* grot, float* gsh, int sms, cudaStream_t stream)
 {
-    const TableShape t = table_shape(g, sms);
+    const TableShape t = table_shape(g, sms, 2);
     grad_pose_kernel<NDIM, INTERP, WIN><<<t.grid, kThreads, t.smem, stream>>>(
-        R, rot, shift, G, grot, gsh, g, (long long)g.n_rec * g.n_pose);
+        R, rot, shift, G, grot, gsh, g, t.splits, t.n_work);
 }
 
 template <int NDIM, int INTERP>
@@ -1226,9 +1268,12 @@ void launch_scatter_tile(const Geom& g, const float2* P, const float* weights, c
     auto kern = scatter_tile_kernel<INTERP, DATA, WTS>;
     cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     const long long n_items = (long long)g.n_rec * g.n_pose;
+    const long long ntiles = (long long)((g.Ho + 3) / 4) * ((g.Do + 3) / 4);
+    const int splits = (int)item_splits(n_items, 3LL * sms, (ntiles + kThreads / 32 - 1) / (kThreads / 32));
+    const long long n_work = n_items * splits;
     const long long cap = 8LL * sms;
-    const unsigned grid = (unsigned)(n_items < cap ? n_items : cap);
-    kern<<<grid, kThreads, smem, stream>>>(P, weights, rot, shift, VO, WO, g, n_items);
+    const unsigned grid = (unsigned)(n_work < cap ? n_work : cap);
+    kern<<<grid, kThreads, smem, stream>>>(P, weights, rot, shift, VO, WO, g, splits, n_work);
 }
 
 template <int NDIM, int INTERP>

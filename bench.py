@@ -54,6 +54,10 @@ def parse():
     ap.add_argument("--cpu-sample", type=int, default=16384, help="poses in the oracle sample")
     ap.add_argument("--batch", type=int, default=None,
                     help="override the workload's batch (small cases for profiling only)")
+    ap.add_argument("--study", choices=["oversampling"], default=None,
+                    help="instead of the step: time the on-the-fly oversampling comparison")
+    ap.add_argument("--study-poses", default="1,16,256,4096,16384",
+                    help="pose counts of the oversampling study")
     return ap.parse_args()
 
 
@@ -392,8 +396,89 @@ def run_ours(args, wl):
     return 0
 
 
+def run_oversampling_study(args):
+    """On-the-fly oversampling against cubic interpolation without it, at D = 128: a real-space
+    volume is zero-padded by 2 and transformed on every pass, then projected with linear
+    weights at c = 2 R q; the alternative transforms the unpadded volume and projects with
+    cubic weights.  'offline' variants start from a precomputed spectrum (projection only).
+    Forward: images from the real-space volume; fwd+bwd adds the gradient of the real-space
+    volume (projection backward, FFT backward, crop).  One JSON line per pose count."""
+    import numpy as np
+    import torch
+    from back_projection_fourier_b300 import synth, tp
+
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    stream = torch.cuda.current_stream(dev)
+    D = 128
+    rng = np.random.default_rng(12345)
+    vol = torch.from_numpy(rng.standard_normal((1, D, D, D)).astype(np.float32)).to(dev)
+    variants = {"cubic_o1": (1, tp.TP_CUBIC), "linear_o2": (2, tp.TP_LINEAR)}
+    bufs = {}
+    for name, (f, interp) in variants.items():
+        P = f * D
+        X = torch.empty((1, P, P, P), device=dev)
+        tp.tp_pad_volume(3, vol, f, X, stream)
+        S = torch.fft.rfftn(X, dim=(-3, -2, -1))
+        bufs[name] = dict(f=f, X=X, S=S, gS=torch.empty_like(S), gvol=torch.empty_like(vol),
+                          op=tp.make_opts(interp, tp.TP_LAYOUT_FFTW, float(f), -1.0))
+    for n_pose in [int(x) for x in args.study_poses.split(",")]:
+        rot = torch.from_numpy(synth.rotations_3d(rng, n_pose)[None]).to(dev)
+        sh = torch.from_numpy(rng.uniform(-5, 5, (1, n_pose, 2)).astype(np.float32)).to(dev)
+        Y = torch.empty((1, n_pose, D, D // 2 + 1), dtype=torch.complex64, device=dev)
+        G = torch.randn((1, n_pose, D, D // 2 + 1), dtype=torch.complex64, device=dev)
+        res = {}
+        for name, b in bufs.items():
+            def fly_fwd(b=b):
+                tp.tp_pad_volume(3, vol, b["f"], b["X"], stream)
+                b["S"] = torch.fft.rfftn(b["X"], dim=(-3, -2, -1))
+                tp.tp_project_3d_to_2d(b["S"], rot, sh, Y, b["op"], stream)
+
+            def fly_fwdbwd(b=b):
+                X = b["X"]
+                tp.tp_pad_volume(3, vol, b["f"], X, stream)
+                Xg = X.detach().requires_grad_(True)
+                S = torch.fft.rfftn(Xg, dim=(-3, -2, -1))
+                tp.tp_project_3d_to_2d(S.detach(), rot, sh, Y, b["op"], stream)
+                tp.tp_project_backward(3, S.detach(), rot, sh, G, b["gS"], None, None, b["op"],
+                                       stream)
+                (gX,) = torch.autograd.grad(S, Xg, b["gS"])
+                tp.tp_crop_volume(3, gX.contiguous(), b["f"], b["gvol"], stream)
+
+            def off_fwd(b=b):
+                tp.tp_project_3d_to_2d(b["S"], rot, sh, Y, b["op"], stream)
+
+            def off_fwdbwd(b=b):
+                tp.tp_project_3d_to_2d(b["S"], rot, sh, Y, b["op"], stream)
+                tp.tp_project_backward(3, b["S"], rot, sh, G, b["gS"], None, None, b["op"], stream)
+
+            for tag, fn in (("fly_fwd", fly_fwd), ("fly_fwdbwd", fly_fwdbwd),
+                            ("offline_fwd", off_fwd), ("offline_fwdbwd", off_fwdbwd)):
+                for _ in range(args.warmup):
+                    fn()
+                torch.cuda.synchronize()
+                t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                t0.record(stream)
+                for _ in range(args.steps):
+                    fn()
+                t1.record(stream)
+                torch.cuda.synchronize()
+                res[f"{name}_{tag}"] = t0.elapsed_time(t1) / args.steps
+        line = {"study": "oversampling", "D": D, "n_pose": n_pose, "unit": "ms per pass",
+                "ms": {k: round(v, 4) for k, v in res.items()},
+                "ratio_fly_fwd": res["linear_o2_fly_fwd"] / res["cubic_o1_fly_fwd"],
+                "ratio_fly_fwdbwd": res["linear_o2_fly_fwdbwd"] / res["cubic_o1_fly_fwdbwd"],
+                "ratio_offline_fwd": res["linear_o2_offline_fwd"] / res["cubic_o1_offline_fwd"],
+                "note": "ratios are linear o=2 time / cubic o=1 time; L2 not flushed (the "
+                        "volumes are re-read every pass, as in training)"}
+        print(json.dumps(line), flush=True)
+    return 0
+
+
 def main():
     args = parse()
+    if args.study == "oversampling":
+        return run_oversampling_study(args)
     from back_projection_fourier_b300 import synth
 
     if args.impl == "reference":
