@@ -51,6 +51,15 @@ def volume_spectrum(rng, D: int, layout=CENTERED, falloff=False) -> np.ndarray:
     return np.ascontiguousarray(_layout(spec, (0, 1), layout).astype(np.complex64))
 
 
+def ball_noise_volume(rng, D: int, margin: int = 2, ndim: int = 3) -> np.ndarray:
+    """Real-space N(0,1) noise inside the ball of radius D/2 - margin about the centre D/2 and
+    zero outside ([D]^ndim, fp64): a synthetic volume whose rotations stay inside the box."""
+    f = rng.standard_normal((D,) * ndim)
+    r = np.indices(f.shape) - D // 2
+    f[(r ** 2).sum(0) > (D // 2 - margin) ** 2] = 0.0
+    return f
+
+
 def image_spectra(rng, n: int, D: int, layout=CENTERED) -> np.ndarray:
     """rfft2 half-images complex64 [n][D][D/2+1] of real N(0,1) images."""
     out = np.empty((n, D, D // 2 + 1), np.complex64)
@@ -152,7 +161,8 @@ class Workload:
         return self.D // 2 + 1
 
 
-# name -> (number, ndim, op, interp, D, B, rc, shift amplitude, falloff)
+# name -> (number, ndim, op, interp, D, B, rc, shift amplitude, falloff[, n_rec])
+# B counts projections; with n_rec > 1 (3D) each reconstruction has B / n_rec poses of its own.
 WORKLOADS = {
     "fwd3d_d32_linear_b64": (1, 3, "fwd", LINEAR, 32, 64, 16.0, 0.0, False),
     "fwdbwd3d_d64_cubic_b4096": (2, 3, "fwdbwd", CUBIC, 64, 4096, 32.0, 5.0, False),
@@ -160,34 +170,38 @@ WORKLOADS = {
     "rot2d_d256_cubic_b8192": (4, 2, "fwdbwd", CUBIC, 256, 8192, 128.0, 8.0, False),
     "fwdbwd3d_d256_cubic_b50000": (5, 3, "fwdbwd", CUBIC, 256, 50000, 128.0, 10.0, True),
     "fwdbwd3d_d128_cubic_b16384": (6, 3, "fwdbwd", CUBIC, 128, 16384, 64.0, 5.0, False),
+    "fwdbwd3d_d128_cubic_r8_b16384": (7, 3, "fwdbwd", CUBIC, 128, 16384, 64.0, 5.0, False, 8),
 }
 
 
 def make_workload(name: str, B: int | None = None, interp: int | None = None,
                   with_grad: bool = True, layout: int = CENTERED) -> Workload:
     """Draw the inputs of a named workload; ``B`` overrides the batch (same recipe)."""
-    number, ndim, op, interp0, D, B0, rc, amp, falloff = WORKLOADS[name]
+    number, ndim, op, interp0, D, B0, rc, amp, falloff, *rest = WORKLOADS[name]
+    n_rec = rest[0] if rest else 1
     B = B0 if B is None else B
+    if B % n_rec:
+        raise ValueError(f"batch {B} is not a multiple of the {n_rec} reconstructions")
     interp = interp0 if interp is None else interp
     seed = 1000 + number
     rng = np.random.default_rng(seed)
     H = D // 2 + 1
     wl = Workload(name, number, ndim, op, interp, D, B, rc, layout)
     if ndim == 3:
-        wl.n_rec, wl.n_pose = 1, B
+        wl.n_rec, wl.n_pose = n_rec, B // n_rec
         if op != "insert":
-            wl.rec = volume_spectrum(rng, D, layout, falloff)[None]
-        wl.rot = rotations_3d(rng, B)[None]
+            wl.rec = np.stack([volume_spectrum(rng, D, layout, falloff) for _ in range(n_rec)])
+        wl.rot = rotations_3d(rng, B).reshape(n_rec, B // n_rec, 3, 3)
     else:
         wl.n_rec, wl.n_pose = B, 1
         wl.rec = image_spectra(rng, B, D, layout)
         wl.rot = rotations_2d(rng, B)[:, None]
     if amp > 0:
         s = shifts(rng, B, amp)
-        wl.shift = s[None] if ndim == 3 else s[:, None]
+        wl.shift = s.reshape(n_rec, B // n_rec, 2) if ndim == 3 else s[:, None]
     if op == "insert" or (op == "fwdbwd" and with_grad):
         g = cn01_items(seed, 1, B, (D, H))
-        wl.grad = g[None] if ndim == 3 else g[:, None]
+        wl.grad = g.reshape(n_rec, B // n_rec, D, H) if ndim == 3 else g[:, None]
     if op == "insert":
         w = ctf_like_weights(D, 40.0, 1e-3, layout)
         wl.weights = np.broadcast_to(w, (wl.n_rec, wl.n_pose, D, H))

@@ -85,7 +85,8 @@ def kernel_hash() -> str:
 # ----------------------------------------------------------------- oracle ----
 
 def oracle_fwdbwd_rate(wl, n_poses: int, nthreads: int) -> tuple[float, str]:
-    """Poses/s of the fp64 oracle's forward + backward on the first n_poses poses."""
+    """Projections/s of the fp64 oracle's forward + backward on the first n_poses poses of
+    every reconstruction."""
     import oracle
 
     n = min(n_poses, wl.n_pose)
@@ -97,7 +98,9 @@ def oracle_fwdbwd_rate(wl, n_poses: int, nthreads: int) -> tuple[float, str]:
     oracle.project(wl.ndim, wl.rec, rot, sh, **kw)
     oracle.project_backward(wl.ndim, wl.rec, rot, g, sh, **kw)
     dt = time.perf_counter() - t0
-    return n / dt, f"first {n} of {wl.n_pose} poses, forward + full backward, fp64, {dt:.1f} s"
+    per = f" of each of {wl.n_rec} reconstructions" if wl.n_rec > 1 else ""
+    return wl.n_rec * n / dt, (f"first {n} of {wl.n_pose} poses{per}, forward + full backward, "
+                               f"fp64, {dt:.1f} s")
 
 
 def run_reference(args, wl):
@@ -105,7 +108,8 @@ def run_reference(args, wl):
     if rank != 0:
         return 0
     nthreads = cores()
-    per_step = max(8, min(args.cpu_sample // 4, wl.n_pose))
+    per_step = max(8, min(args.cpu_sample // 4 // wl.n_rec, wl.n_pose))
+    items = per_step * wl.n_rec
     import oracle
 
     oracle.build()
@@ -115,12 +119,12 @@ def run_reference(args, wl):
     for _ in range(args.steps):
         oracle_fwdbwd_rate(wl, per_step, nthreads)
     dt = time.perf_counter() - t0
-    value = per_step * args.steps / dt
-    sample = f"{per_step} of {wl.n_pose} poses per step (forward + full backward, fp64)"
+    value = items * args.steps / dt
+    sample = f"{items} of {wl.B} projections per step (forward + full backward, fp64)"
     line = {
         "impl": "reference", "metric": METRIC, "value": value, "unit": "projections/s",
         "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
-        "ms_per_step": 1e3 * dt / args.steps * (wl.n_pose / per_step),
+        "ms_per_step": 1e3 * dt / args.steps * (wl.B / items),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
         "data": "synthetic", "config": workload_config(wl, "n/a (host oracle)"),
         "cpu_baseline": {"value": value, "unit": "projections/s", "cores": nthreads,
@@ -187,7 +191,8 @@ class ClockSampler:
 # ------------------------------------------------------------------ ours ----
 
 def workload_config(wl, l2: str) -> dict:
-    return {"workload": wl.name, "D": wl.D, "batch": wl.B, "interp": "cubic" if wl.interp else "linear",
+    return {"workload": wl.name, "D": wl.D, "batch": wl.B, "n_rec": wl.n_rec,
+            "interp": "cubic" if wl.interp else "linear",
             "cutoff": wl.rc, "shift_amp": wl.extra["shift_amp"],
             "layout": "centered" if wl.layout else "fftw", "step": "forward + fused backward",
             "l2": l2}

@@ -15,6 +15,7 @@ from .oracle import (  # noqa: F401
     oversampled_spectrum,
     project_real,
     project_real_backward,
+    exact_projection,
     axis_weights,
     LINEAR,
     CUBIC,

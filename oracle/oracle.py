@@ -294,6 +294,51 @@ def project_real_backward(ndim, vol, rot, grad_out, shift=None, factor=1, interp
     return crop_volume(g_x, D), g_rot, g_sh
 
 
+def exact_projection(ndim, vol, rot, shift=None, Do=None, cutoff=-1.0):
+    """Ground truth of the projection of a real-space volume: its Fourier transform evaluated
+    exactly (no interpolation) at c = R q for every kept pixel,
+        F(c) = sum_n v[n] exp(-2 pi i c . (n - D/2) / D),
+    times the shift phase exp(-2 pi i (kx sx + ky sy) / Do), in FFTW layout.  This is the
+    reference of the accuracy comparison (Spanish page, results, precision bullet: Fourier
+    ring correlation and real-space intensity attenuation of cubic without oversampling
+    against linear with 2x oversampling).  vol: [n][D]^ndim real, centre at index D/2; rot:
+    [n_rot][n_pose][k][k]; shift as in project().  Cost D^ndim per pixel (matrix products
+    over one axis at a time)."""
+    vol = np.asarray(vol, np.float64)
+    rot = np.asarray(rot, np.float64)
+    n, D = vol.shape[0], vol.shape[-1]
+    Do = D if Do is None else Do
+    Ho = Do // 2 + 1
+    n_rot, n_pose = rot.shape[:2]
+    rc = Do / 2 if cutoff < 0 else cutoff
+    ky = np.fft.fftfreq(Do, 1.0 / Do)
+    KY, KX = np.meshgrid(ky, np.arange(Ho), indexing="ij")
+    keep = KX * KX + KY * KY <= np.floor(rc * rc)
+    q = np.stack([KX[keep], KY[keep]], 0)
+    m = np.arange(D) - D // 2
+    out = np.zeros((n, n_pose, Do, Ho), np.complex128)
+    for r in range(n):
+        for p in range(n_pose):
+            R = rot[0 if n_rot == 1 else r, p]
+            c = R[:, :2] @ q                      # (k, P): vector order x, y[, z]
+            E = [np.exp(-2j * np.pi * np.outer(c[a], m) / D) for a in range(ndim)]
+            if ndim == 3:
+                t = vol[r].reshape(D * D, D) @ E[0].T            # (z*y, P)
+                t = np.einsum("zyp,py->zp", t.reshape(D, D, -1), E[1])
+                val = np.einsum("zp,pz->p", t, E[2])
+            else:
+                t = vol[r] @ E[0].T                               # (y, P)
+                val = np.einsum("yp,py->p", t, E[1])
+            if shift is not None:
+                sh = np.asarray(shift, np.float64)
+                s = sh[0 if sh.shape[0] == 1 else r, p]
+                val = val * np.exp(-2j * np.pi * (q[0] * s[0] + q[1] * s[1]) / Do)
+            img = np.zeros((Do, Ho), np.complex128)
+            img[keep] = val
+            out[r, p] = img
+    return out
+
+
 def axis_weights(c: float, interp=CUBIC):
     """Taps, kernel weights and kernel derivatives of one axis at coordinate c."""
     t = np.zeros(4, np.int64)

@@ -12,14 +12,14 @@ import torch.multiprocessing as mp
 from back_projection_fourier_b300.shard import pose_range
 
 
-def _worker(rank, world, port, res):
+def _worker(rank, world, port, res, name, B):
     os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port))
     dist.init_process_group("gloo", rank=rank, world_size=world)
     try:
         import oracle
         from back_projection_fourier_b300 import synth
 
-        wl = synth.make_workload("fwdbwd3d_d64_cubic_b4096", B=23)
+        wl = synth.make_workload(name, B=B)
         kw = dict(interp=wl.interp, layout=wl.layout, cutoff=wl.rc, nthreads=1)
         a, b = pose_range(wl.n_pose, rank, world)
         sl = lambda x: None if x is None else np.ascontiguousarray(x[:, a:b])  # noqa: E731
@@ -55,14 +55,19 @@ def test_pose_range_partitions():
         pose_range(5, 2, 2)
 
 
-def test_two_rank_gloo_sharding_matches_unsharded():
+@pytest.mark.parametrize("name,B", [("fwdbwd3d_d64_cubic_b4096", 23),
+                                    ("fwdbwd3d_d128_cubic_r8_b16384", 24)])
+def test_two_rank_gloo_sharding_matches_unsharded(name, B):
+    """Shards of every reconstruction's poses; with several reconstructions each rank
+    all-reduces all of their gradient volumes at once."""
     import oracle
     oracle.build()
     ctx = mp.get_context("spawn")
     with ctx.Manager() as m:
         res = m.dict()
-        port = 29500 + os.getpid() % 1000
-        mp.start_processes(_worker, args=(2, port, res), nprocs=2, join=True, start_method="spawn")
+        port = 29500 + (os.getpid() + B) % 1000
+        mp.start_processes(_worker, args=(2, port, res, name, B), nprocs=2, join=True,
+                           start_method="spawn")
         res = dict(res)
     assert res["rec"] < 1e-13 and res["vol"] < 1e-13 and res["wvol"] < 1e-13, res
     assert res["fwd_shard0"] == 0.0 and res["rot_shard0"] == 0.0, res

@@ -108,15 +108,16 @@ def _fwdbwd3d_sampled(name, n_pix=6000, n_poses=48):
     y = tp.project(V, R, S, opts=op)
     g_rec, g_rot, g_sh = tp.project_backward(V, R, G, S, opts=op)
     rng = np.random.default_rng(11)
-    items = rng.integers(0, wl.B, n_pix)
+    n_items = wl.n_rec * wl.n_pose
+    items = rng.integers(0, n_items, n_pix)
     pix = rng.integers(0, wl.D * wl.H, n_pix)
-    got = y.reshape(wl.B, -1)[torch.from_numpy(items).cuda(), torch.from_numpy(pix).cuda()]
+    got = y.reshape(n_items, -1)[torch.from_numpy(items).cuda(), torch.from_numpy(pix).cuda()]
     ref = oracle.project_samples(3, wl.rec, wl.rot, items, pix, wl.shift, **kw)
     # relative to the largest output value of the whole projection stack
     scale = float(y.abs().max())
     assert float(np.abs(host(got) - ref).max()) <= TOL_FWD * scale
     # rotation / shift gradients of sampled poses depend on those poses alone
-    poses = np.sort(rng.choice(wl.B, n_poses, replace=False))
+    poses = np.sort(rng.choice(wl.n_pose, n_poses // wl.n_rec, replace=False))
     _, r_rot, r_sh = oracle.project_backward(3, wl.rec, sub(wl.rot, poses), sub(wl.grad, poses),
                                              sub(wl.shift, poses), want_rec=False, **kw)
     tpo = torch.from_numpy(poses).cuda()
@@ -130,6 +131,12 @@ def _fwdbwd3d_sampled(name, n_pix=6000, n_poses=48):
 
 def test_fwdbwd3d_d128_cubic_full_sampled():
     _fwdbwd3d_sampled("fwdbwd3d_d128_cubic_b16384")
+
+
+def test_fwdbwd3d_d128_cubic_r8_full_sampled():
+    """Eight reconstructions, each with 2048 poses of its own (per-reconstruction rotations
+    and shifts): items index (reconstruction, pose), gradients land in their own volume."""
+    _fwdbwd3d_sampled("fwdbwd3d_d128_cubic_r8_b16384")
 
 
 def test_fwdbwd3d_d256_cubic_full_sampled():
