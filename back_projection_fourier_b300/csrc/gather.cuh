@@ -15,11 +15,16 @@
 // The window's alignment shift depends only on the y row (the z plane stride Dv*Hv is a
 // multiple of the window for WIN = 2, and of 4 elements when Dv % 4 == 0, which the host
 // requires for WIN = 4), so the shifted x weights are formed once per y tap.
+//   WIN = kGrouped: rows read from the grouped copy of the volume (see expand_groups in
+//   kernels.cu), where element NT*i + k holds tap i + k: one aligned 32-byte (cubic) or
+//   16-byte (linear) load per row, always within one sector.
 #pragma once
 
 #include "tp_device.cuh"
 
 namespace tp {
+
+constexpr int kGrouped = 8;  // WIN tag of the grouped-row reader
 
 template <int WIN>
 struct Window;
@@ -243,7 +248,47 @@ struct RowReader<INTERP, 4, DERIV> {
     }
 };
 
-// v (and dv when DERIV) in the effective frame: sum over rows (z tap a, y tap b).
+// Grouped rows: p points at a group of NT consecutive taps (32-byte aligned for cubic,
+// 16-byte aligned for linear).
+template <int INTERP, bool DERIV>
+struct RowReader<INTERP, kGrouped, DERIV> {
+    static constexpr int NT = Taps<INTERP>::N;
+    static constexpr int NW = NT;
+    __device__ __forceinline__ static int shift(const float2*, int) { return 0; }
+    __device__ __forceinline__ static void shifted(int, const float* w, float* ws)
+    {
+#pragma unroll
+        for (int k = 0; k < NT; ++k) ws[k] = w[k];
+    }
+    __device__ __forceinline__ static void read(const float2* __restrict__ p, int, const float* ws,
+                                                const float* wds, float2& rs, float2& rsd)
+    {
+        float e[2 * NT];
+        if constexpr (NT == 4) {
+            ldg_v8(p, e);
+        } else {
+            const float4 v = ldg_v4(p);
+            e[0] = v.x;
+            e[1] = v.y;
+            e[2] = v.z;
+            e[3] = v.w;
+        }
+        rs = make_float2(0.f, 0.f);
+        rsd = make_float2(0.f, 0.f);
+#pragma unroll
+        for (int j = 0; j < NT; ++j) {
+            rs.x = fmaf(ws[j], e[2 * j], rs.x);
+            rs.y = fmaf(ws[j], e[2 * j + 1], rs.y);
+            if constexpr (DERIV) {
+                rsd.x = fmaf(wds[j], e[2 * j], rsd.x);
+                rsd.y = fmaf(wds[j], e[2 * j + 1], rsd.y);
+            }
+        }
+    }
+};
+
+// v (and dv when DERIV) in the effective frame: sum over rows (z tap a, y tap b).  With
+// WIN = kGrouped, V is the item's grouped volume (NT elements per voxel).
 template <int NDIM, int INTERP, int WIN, bool DERIV>
 __device__ __forceinline__ void gather_fast(const float2* __restrict__ V,
                                             const FastTaps<NDIM, INTERP, DERIV>& t, float2& v,
@@ -254,7 +299,8 @@ __device__ __forceinline__ void gather_fast(const float2* __restrict__ V,
     constexpr int NZ = NDIM == 3 ? NT : 1;
     v = make_float2(0.f, 0.f);
     if constexpr (DERIV) dv[0] = dv[1] = dv[2] = make_float2(0.f, 0.f);
-    const float2* Vx = V + t.x0;
+    constexpr int M = WIN == kGrouped ? NT : 1;  // elements per voxel of V
+    const float2* Vx = V + M * t.x0;
 #pragma unroll
     for (int b = 0; b < NT; ++b) {
         // the window shift depends on the y row only (plane strides keep the alignment)
@@ -265,7 +311,7 @@ __device__ __forceinline__ void gather_fast(const float2* __restrict__ V,
 #pragma unroll
         for (int a = 0; a < NZ; ++a) {
             float2 rs, rsd;
-            RR::read(Vx + t.zoff[a] + t.yrow[b], s, ws, wds, rs, rsd);
+            RR::read(Vx + M * (t.zoff[a] + t.yrow[b]), s, ws, wds, rs, rsd);
             const float wzy = t.wz[a] * t.wy[b];
             v.x = fmaf(wzy, rs.x, v.x);
             v.y = fmaf(wzy, rs.y, v.y);

@@ -195,7 +195,8 @@ __device__ __forceinline__ bool eval_fast(const Geom& g, const float2* __restric
 template <int NDIM, int INTERP, int WIN>
 __global__ void __launch_bounds__(kThreads, 4) project_kernel(
     const float2* __restrict__ rec, const float* __restrict__ rot,
-    const float* __restrict__ shift, float2* __restrict__ out, Geom g, int splits, long long n_work)
+    const float* __restrict__ shift, float2* __restrict__ out, Geom g, int splits, long long n_work,
+    const float2* __restrict__ grouped)
 {
     extern __shared__ int smem[];
     int* rowstart = smem;                    // [Do + 1]
@@ -216,6 +217,7 @@ __global__ void __launch_bounds__(kThreads, 4) project_kernel(
         ItemParams<NDIM> ip;
         load_item<NDIM>(g, rot, shift, ir.r, ir.p, ip);
         const float2* V = rec + (long long)ir.r * g.rec_elems;
+        const float2* VG = WIN == kGrouped ? grouped + (long long)Taps<INTERP>::N * ir.r * g.rec_elems : V;
         float2* y = out + ir.item * g.img_elems;
         // pixels beyond the cutoff are zero
         for (int p = ir.part * kThreads + threadIdx.x; p < npix; p += splits * kThreads) {
@@ -240,7 +242,8 @@ __global__ void __launch_bounds__(kThreads, 4) project_kernel(
                 kx = n - rowstart[row];
                 const int ky = row_freq(row, g.Do, g.halfo, g.centered);
                 float2 v;
-                if (eval_fast<NDIM, INTERP, WIN, false>(g, V, ip.R, kx, ky, v, nullptr))
+                if (eval_fast<NDIM, INTERP, WIN, false>(g, WIN == kGrouped ? VG : V, ip.R, kx, ky, v,
+                                                        nullptr))
                     finish(row, kx, v);
                 else
                     slow = true;
@@ -326,7 +329,8 @@ template <int NDIM, int INTERP, int WIN>
 __global__ void __launch_bounds__(kThreads) grad_pose_kernel(
     const float2* __restrict__ rec, const float* __restrict__ rot,
     const float* __restrict__ shift, const float2* __restrict__ gout,
-    float* __restrict__ grot, float* __restrict__ gsh, Geom g, int splits, long long n_work)
+    float* __restrict__ grot, float* __restrict__ gsh, Geom g, int splits, long long n_work,
+    const float2* __restrict__ grouped)
 {
     constexpr int NG = NDIM * 2 + 2;
     extern __shared__ int smem[];
@@ -348,6 +352,7 @@ __global__ void __launch_bounds__(kThreads) grad_pose_kernel(
         ItemParams<NDIM> ip;
         load_item<NDIM>(g, rot, shift, ir.r, ir.p, ip);
         const float2* V = rec + (long long)ir.r * g.rec_elems;
+        const float2* VG = WIN == kGrouped ? grouped + (long long)Taps<INTERP>::N * ir.r * g.rec_elems : V;
         const float2* gy = gout + ir.item * g.img_elems;
         float acc[NG];
 #pragma unroll
@@ -370,7 +375,7 @@ __global__ void __launch_bounds__(kThreads) grad_pose_kernel(
                 kx = n - rowstart[row];
                 const int ky = row_freq(row, g.Do, g.halfo, g.centered);
                 float2 v, dv[3];
-                if (eval_fast<NDIM, INTERP, WIN, true>(g, V, ip.R, kx, ky, v, dv))
+                if (eval_fast<NDIM, INTERP, WIN, true>(g, WIN == kGrouped ? VG : V, ip.R, kx, ky, v, dv))
                     add(row, kx, v, dv);
                 else
                     slow = true;
@@ -1152,6 +1157,25 @@ LaunchShape launch_shape(const Geom& g, int sms)
     return s;
 }
 
+// Grouped copy of the volumes for the gathers: for every voxel (row, x) the NT taps
+// x .. x + NT - 1 of its row, zero past the stored half axis x = Dv/2.  Layout
+// [n_rec][Dv][Dv][Hv][NT] complex; a row's taps are then one aligned vector load.  One CTA
+// per volume row at a time, threads over the row's NT * Hv outputs (coalesced stores).
+template <int NT>
+__global__ void __launch_bounds__(kThreads) expand_groups_kernel(const float2* __restrict__ V,
+                                                                  float2* __restrict__ Q, int Hv,
+                                                                  int halfv, long long rows)
+{
+    for (long long row = blockIdx.x; row < rows; row += gridDim.x) {
+        const float2* v = V + row * Hv;
+        float2* q = Q + row * Hv * NT;
+        for (int e = threadIdx.x; e < Hv * NT; e += kThreads) {
+            const int x = e / NT, k = e - x * NT;
+            q[e] = x + k <= halfv ? __ldg(v + x + k) : make_float2(0.f, 0.f);
+        }
+    }
+}
+
 // Splits of one item over CTAs so that a small batch still fills `target` CTAs: at most
 // `max_parts` (the item's units of work), at least 1.
 long long item_splits(long long n_items, long long target, long long max_parts)
@@ -1191,16 +1215,16 @@ int window_for(const Geom& g, int ndim) { return (ndim == 2 || g.Dv % 4 == 0) ? 
 
 template <int NDIM, int INTERP, int WIN>
 void launch_project_table(const Geom& g, const float2* R, const float* rot, const float* shift,
-                          float2* Y, int sms, cudaStream_t stream)
+                          float2* Y, const float2* grouped, int sms, cudaStream_t stream)
 {
     const TableShape t = table_shape(g, sms, 4);
     project_kernel<NDIM, INTERP, WIN><<<t.grid, kThreads, t.smem, stream>>>(
-        R, rot, shift, Y, g, t.splits, t.n_work);
+        R, rot, shift, Y, g, t.splits, t.n_work, grouped);
 }
 
 template <int NDIM, int INTERP>
 void launch_project_t(const Geom& g, const float2* R, const float* rot, const float* shift,
-                      float2* Y, int sms, cudaStream_t stream)
+                      float2* Y, const float2* grouped, int sms, cudaStream_t stream)
 {
     if (!use_table(g)) {
         const LaunchShape s = launch_shape(g, sms);
@@ -1208,26 +1232,30 @@ void launch_project_t(const Geom& g, const float2* R, const float* rot, const fl
                                                                            s.splits, s.n_work);
         return;
     }
-    if (window_for(g, NDIM) == 4)
-        launch_project_table<NDIM, INTERP, 4>(g, R, rot, shift, Y, sms, stream);
+    if (grouped)
+        launch_project_table<NDIM, INTERP, kGrouped>(g, R, rot, shift, Y, grouped, sms, stream);
+    else if (window_for(g, NDIM) == 4)
+        launch_project_table<NDIM, INTERP, 4>(g, R, rot, shift, Y, nullptr, sms, stream);
     else if (window_for(g, NDIM) == 2)
-        launch_project_table<NDIM, INTERP, 2>(g, R, rot, shift, Y, sms, stream);
+        launch_project_table<NDIM, INTERP, 2>(g, R, rot, shift, Y, nullptr, sms, stream);
     else
-        launch_project_table<NDIM, INTERP, 1>(g, R, rot, shift, Y, sms, stream);
+        launch_project_table<NDIM, INTERP, 1>(g, R, rot, shift, Y, nullptr, sms, stream);
 }
 
 template <int NDIM, int INTERP, int WIN>
 void launch_grad_table(const Geom& g, const float2* R, const float* rot, const float* shift,
-                       const float2* G, float* grot, float* gsh, int sms, cudaStream_t stream)
+                       const float2* G, float* grot, float* gsh, const float2* grouped, int sms,
+                       cudaStream_t stream)
 {
     const TableShape t = table_shape(g, sms, 2);
     grad_pose_kernel<NDIM, INTERP, WIN><<<t.grid, kThreads, t.smem, stream>>>(
-        R, rot, shift, G, grot, gsh, g, t.splits, t.n_work);
+        R, rot, shift, G, grot, gsh, g, t.splits, t.n_work, grouped);
 }
 
 template <int NDIM, int INTERP>
 void launch_grad_t(const Geom& g, const float2* R, const float* rot, const float* shift,
-                   const float2* G, float* grot, float* gsh, int sms, cudaStream_t stream)
+                   const float2* G, float* grot, float* gsh, const float2* grouped, int sms,
+                   cudaStream_t stream)
 {
     if (!use_table(g)) {
         const LaunchShape s = launch_shape(g, sms);
@@ -1235,12 +1263,14 @@ void launch_grad_t(const Geom& g, const float2* R, const float* rot, const float
             R, rot, shift, G, grot, gsh, g, s.splits, s.n_work);
         return;
     }
-    if (window_for(g, NDIM) == 4)
-        launch_grad_table<NDIM, INTERP, 4>(g, R, rot, shift, G, grot, gsh, sms, stream);
+    if (grouped)
+        launch_grad_table<NDIM, INTERP, kGrouped>(g, R, rot, shift, G, grot, gsh, grouped, sms, stream);
+    else if (window_for(g, NDIM) == 4)
+        launch_grad_table<NDIM, INTERP, 4>(g, R, rot, shift, G, grot, gsh, nullptr, sms, stream);
     else if (window_for(g, NDIM) == 2)
-        launch_grad_table<NDIM, INTERP, 2>(g, R, rot, shift, G, grot, gsh, sms, stream);
+        launch_grad_table<NDIM, INTERP, 2>(g, R, rot, shift, G, grot, gsh, nullptr, sms, stream);
     else
-        launch_grad_table<NDIM, INTERP, 1>(g, R, rot, shift, G, grot, gsh, sms, stream);
+        launch_grad_table<NDIM, INTERP, 1>(g, R, rot, shift, G, grot, gsh, nullptr, sms, stream);
 }
 
 template <int NDIM, int INTERP, bool DATA, bool WTS>
@@ -1337,43 +1367,60 @@ cudaError_t launch_weights_grad(int ndim, int interp, const Geom& g, const float
     return cudaGetLastError();
 }
 
+cudaError_t launch_expand_groups(int interp, const Geom& g, const void* rec, void* grouped, int sms,
+                                 cudaStream_t stream)
+{
+    const long long rows = (long long)g.n_rec * g.Dv * g.Dv;
+    if (rows == 0) return cudaSuccess;
+    const unsigned grid = (unsigned)(rows < 16LL * sms ? rows : 16LL * sms);
+    auto V = static_cast<const float2*>(rec);
+    auto Q = static_cast<float2*>(grouped);
+    if (interp == kCubic)
+        expand_groups_kernel<4><<<grid, kThreads, 0, stream>>>(V, Q, g.Hv, g.halfv, rows);
+    else
+        expand_groups_kernel<2><<<grid, kThreads, 0, stream>>>(V, Q, g.Hv, g.halfv, rows);
+    return cudaGetLastError();
+}
+
 cudaError_t launch_project(int ndim, int interp, const Geom& g, const void* rec,
                            const float* rot, const float* shift, void* out, int sms,
-                           cudaStream_t stream)
+                           cudaStream_t stream, const void* grouped)
 {
     if ((long long)g.n_rec * g.n_pose == 0) return cudaSuccess;
     auto R = static_cast<const float2*>(rec);
     auto Y = static_cast<float2*>(out);
+    auto Q = static_cast<const float2*>(grouped);
     if (ndim == 3 && interp == kCubic)
-        launch_project_t<3, kCubic>(g, R, rot, shift, Y, sms, stream);
+        launch_project_t<3, kCubic>(g, R, rot, shift, Y, Q, sms, stream);
     else if (ndim == 3)
-        launch_project_t<3, kLinear>(g, R, rot, shift, Y, sms, stream);
+        launch_project_t<3, kLinear>(g, R, rot, shift, Y, Q, sms, stream);
     else if (interp == kCubic)
-        launch_project_t<2, kCubic>(g, R, rot, shift, Y, sms, stream);
+        launch_project_t<2, kCubic>(g, R, rot, shift, Y, nullptr, sms, stream);
     else
-        launch_project_t<2, kLinear>(g, R, rot, shift, Y, sms, stream);
+        launch_project_t<2, kLinear>(g, R, rot, shift, Y, nullptr, sms, stream);
     return cudaGetLastError();
 }
 
 cudaError_t launch_backward(int ndim, int interp, const Geom& g, const void* rec,
                             const float* rot, const float* shift, const void* grad_out,
                             void* grad_rec, float* grad_rot, float* grad_shift, int sms,
-                            cudaStream_t stream)
+                            cudaStream_t stream, const void* grouped)
 {
     if ((long long)g.n_rec * g.n_pose == 0) return cudaSuccess;
     auto R = static_cast<const float2*>(rec);
     auto G = static_cast<const float2*>(grad_out);
     auto GR = static_cast<float2*>(grad_rec);
+    auto Q = static_cast<const float2*>(grouped);
     const bool want_grad = grad_rot || (grad_shift && g.has_shift);
     if (want_grad) {
         if (ndim == 3 && interp == kCubic)
-            launch_grad_t<3, kCubic>(g, R, rot, shift, G, grad_rot, grad_shift, sms, stream);
+            launch_grad_t<3, kCubic>(g, R, rot, shift, G, grad_rot, grad_shift, Q, sms, stream);
         else if (ndim == 3)
-            launch_grad_t<3, kLinear>(g, R, rot, shift, G, grad_rot, grad_shift, sms, stream);
+            launch_grad_t<3, kLinear>(g, R, rot, shift, G, grad_rot, grad_shift, Q, sms, stream);
         else if (interp == kCubic)
-            launch_grad_t<2, kCubic>(g, R, rot, shift, G, grad_rot, grad_shift, sms, stream);
+            launch_grad_t<2, kCubic>(g, R, rot, shift, G, grad_rot, grad_shift, nullptr, sms, stream);
         else
-            launch_grad_t<2, kLinear>(g, R, rot, shift, G, grad_rot, grad_shift, sms, stream);
+            launch_grad_t<2, kLinear>(g, R, rot, shift, G, grad_rot, grad_shift, nullptr, sms, stream);
     }
     if (GR) {
         if (ndim == 3 && interp == kCubic)

@@ -9,14 +9,20 @@ namespace tp {
 
 // Each launcher enqueues on `stream` and returns cudaGetLastError().  Arguments have been
 // validated by the ABI layer; `sms` is the device's SM count (grid sizing).
+// `grouped` (3D only; NULL = read rec directly): the grouped copy of rec written by
+// launch_expand_groups, read by the gathers' fast path.
 cudaError_t launch_project(int ndim, int interp, const Geom& g, const void* rec,
                            const float* rot, const float* shift, void* out, int sms,
-                           cudaStream_t stream);
+                           cudaStream_t stream, const void* grouped = nullptr);
 
 cudaError_t launch_backward(int ndim, int interp, const Geom& g, const void* rec,
                             const float* rot, const float* shift, const void* grad_out,
                             void* grad_rec, float* grad_rot, float* grad_shift, int sms,
-                            cudaStream_t stream);
+                            cudaStream_t stream, const void* grouped = nullptr);
+
+// Grouped copy of the volumes: [n_rec][Dv][Dv][Hv][NT] complex, NT = 4 (cubic) / 2 (linear).
+cudaError_t launch_expand_groups(int interp, const Geom& g, const void* rec, void* grouped, int sms,
+                                 cudaStream_t stream);
 
 cudaError_t launch_backproject(int ndim, int interp, const Geom& g, const void* proj,
                                const float* weights, const float* rot, const float* shift,

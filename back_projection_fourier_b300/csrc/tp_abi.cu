@@ -1,6 +1,7 @@
 // tp_abi.cu -- the extern "C" entry points of libtp.so declared in include/tp.h:
 // argument validation on the host, derived geometry, output zeroing and the launches.
 #include <cmath>
+#include <cstddef>
 #include <cstdint>
 #include <climits>
 
@@ -91,14 +92,42 @@ int sm_count()
     return sms > 0 ? sms : 148;
 }
 
+// Bytes of the grouped-volume workspace of the 3D gathers (0: not used).  The gathers index
+// it with 32-bit offsets, so NT * (elements of one volume) must stay below 2^31.
+size_t grouped_bytes(int ndim, int n_rec, int Dv, int interp)
+{
+    if (ndim != 3 || n_rec <= 0 || !box_ok(Dv, 3)) return 0;
+    const long long nt = interp == TP_CUBIC ? 4 : 2;
+    const long long per = (long long)Dv * Dv * (Dv / 2 + 1) * nt;
+    if (per >= (1LL << 31)) return 0;
+    return (size_t)(per * n_rec * 8);
+}
+
+// Checks a caller's workspace; sets `use` when the gathers will read the grouped copy.
+tp_status check_workspace(int ndim, int n_rec, int Dv, int interp, const void* ws, size_t ws_bytes,
+                          bool& use)
+{
+    use = false;
+    if (!ws) return TP_OK;
+    const size_t need = grouped_bytes(ndim, n_rec, Dv, interp);
+    if (need == 0) return TP_OK;
+    if (ws_bytes < need) return TP_ERR_SHAPE;
+    if (!aligned(ws, 32)) return TP_ERR_VALUE;
+    use = true;
+    return TP_OK;
+}
+
 tp_status project_impl(int ndim, const void* rec, int n_rec, int Dv, const float* rot,
                        int n_rot, int n_pose, const float* shift, int n_sh, void* out, int Do,
-                       const tp_opts* opts, void* stream)
+                       const tp_opts* opts, void* stream, void* ws = nullptr, size_t ws_bytes = 0)
 {
     Opts o;
     tp_status st = read_opts(opts, o);
     if (st != TP_OK) return st;
     st = check_common(ndim, n_rec, Dv, Do, n_rot, n_pose, shift, n_sh);
+    if (st != TP_OK) return st;
+    bool use_ws = false;
+    st = check_workspace(ndim, n_rec, Dv, o.interp, ws, ws_bytes, use_ws);
     if (st != TP_OK) return st;
     const long long n_items = (long long)n_rec * n_pose;
     if (n_items == 0) return TP_OK;
@@ -106,8 +135,12 @@ tp_status project_impl(int ndim, const void* rec, int n_rec, int Dv, const float
     if (!aligned(rec, 8) || !aligned(out, 8) || !aligned(rot, 4) || (shift && !aligned(shift, 4)))
         return TP_ERR_VALUE;
     const tp::Geom g = make_geom(ndim, n_rec, Dv, n_rot, n_pose, shift, n_sh, Do, o);
-    const cudaError_t e = tp::launch_project(ndim, o.interp, g, rec, rot, shift, out, sm_count(),
-                                             static_cast<cudaStream_t>(stream));
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    const int sms = sm_count();
+    cudaError_t e = cudaSuccess;
+    if (use_ws) e = tp::launch_expand_groups(o.interp, g, rec, ws, sms, s);
+    if (e == cudaSuccess)
+        e = tp::launch_project(ndim, o.interp, g, rec, rot, shift, out, sms, s, use_ws ? ws : nullptr);
     return e == cudaSuccess ? TP_OK : TP_ERR_CUDA;
 }
 
@@ -156,6 +189,22 @@ tp_status tp_project_3d_to_2d(const void* vol, int n_rec, int Dv, const float* r
     return project_impl(3, vol, n_rec, Dv, rot, n_rot, n_pose, shift, n_sh, out, Do, opts, stream);
 }
 
+tp_status tp_project_3d_to_2d_ws(const void* vol, int n_rec, int Dv, const float* rot, int n_rot,
+                                 int n_pose, const float* shift, int n_sh, void* out, int Do,
+                                 void* workspace, size_t workspace_bytes, const tp_opts* opts,
+                                 void* stream)
+{
+    return project_impl(3, vol, n_rec, Dv, rot, n_rot, n_pose, shift, n_sh, out, Do, opts, stream,
+                        workspace, workspace_bytes);
+}
+
+size_t tp_workspace_size(int ndim, int n_rec, int Dv, const tp_opts* opts)
+{
+    Opts o;
+    if (read_opts(opts, o) != TP_OK) return 0;
+    return grouped_bytes(ndim, n_rec, Dv, o.interp);
+}
+
 tp_status tp_project_2d_to_2d(const void* img, int n_rec, int Dv, const float* rot, int n_rot,
                               int n_pose, const float* shift, int n_sh, void* out, int Do,
                               const tp_opts* opts, void* stream)
@@ -186,10 +235,23 @@ tp_status tp_project_backward(int ndim, const void* rec, int n_rec, int Dv, cons
                               const void* grad_out, int Do, void* grad_rec, float* grad_rot,
                               float* grad_shift, const tp_opts* opts, void* stream)
 {
+    return tp_project_backward_ws(ndim, rec, n_rec, Dv, rot, n_rot, n_pose, shift, n_sh, grad_out,
+                                  Do, grad_rec, grad_rot, grad_shift, nullptr, 0, opts, stream);
+}
+
+tp_status tp_project_backward_ws(int ndim, const void* rec, int n_rec, int Dv, const float* rot,
+                                 int n_rot, int n_pose, const float* shift, int n_sh,
+                                 const void* grad_out, int Do, void* grad_rec, float* grad_rot,
+                                 float* grad_shift, void* workspace, size_t workspace_bytes,
+                                 const tp_opts* opts, void* stream)
+{
     Opts o;
     tp_status st = read_opts(opts, o);
     if (st != TP_OK) return st;
     st = check_common(ndim, n_rec, Dv, Do, n_rot, n_pose, shift, n_sh);
+    if (st != TP_OK) return st;
+    bool use_ws = false;
+    st = check_workspace(ndim, n_rec, Dv, o.interp, workspace, workspace_bytes, use_ws);
     if (st != TP_OK) return st;
     const long long n_items = (long long)n_rec * n_pose;
     const bool want_grad = grad_rot || (grad_shift && shift);
@@ -214,8 +276,13 @@ tp_status tp_project_backward(int ndim, const void* rec, int n_rec, int Dv, cons
     if (grad_shift && cudaMemsetAsync(grad_shift, 0, n_sh_rows * n_pose * 2 * 4, s) != cudaSuccess)
         return TP_ERR_CUDA;
     if (n_items == 0 || (!grad_rec && !want_grad)) return TP_OK;
-    const cudaError_t e = tp::launch_backward(ndim, o.interp, g, rec, rot, shift, grad_out,
-                                              grad_rec, grad_rot, grad_shift, sm_count(), s);
+    const int sms = sm_count();
+    use_ws = use_ws && want_grad;  // only the pose-gradient gather reads the grouped copy
+    cudaError_t e = cudaSuccess;
+    if (use_ws) e = tp::launch_expand_groups(o.interp, g, rec, workspace, sms, s);
+    if (e == cudaSuccess)
+        e = tp::launch_backward(ndim, o.interp, g, rec, rot, shift, grad_out, grad_rec, grad_rot,
+                                grad_shift, sms, s, use_ws ? workspace : nullptr);
     return e == cudaSuccess ? TP_OK : TP_ERR_CUDA;
 }
 

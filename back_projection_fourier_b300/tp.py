@@ -52,13 +52,19 @@ def _load() -> ctypes.CDLL:
     L.tp_backproject_2d_to_2d.argtypes = [P, P, I, I, P, I, I, P, I, P, P, I, I, O, P]
     L.tp_project_backward.argtypes = [I, P, I, I, P, I, I, P, I, P, I, P, P, P, O, P]
     L.tp_backproject_backward.argtypes = [I, P, P, I, I, P, I, I, P, I, P, P, I, P, P, P, P, O, P]
+    Z = ctypes.c_size_t
+    L.tp_workspace_size.argtypes = [I, I, I, O]
+    L.tp_workspace_size.restype = Z
+    L.tp_project_3d_to_2d_ws.argtypes = [P, I, I, P, I, I, P, I, P, I, P, Z, O, P]
+    L.tp_project_backward_ws.argtypes = [I, P, I, I, P, I, I, P, I, P, I, P, P, P, P, Z, O, P]
     L.tp_pad_volume.argtypes = [I, P, I, I, I, P, P]
     L.tp_crop_volume.argtypes = [I, P, I, I, I, P, P]
     L.tp_status_string.argtypes = [I]
     L.tp_status_string.restype = ctypes.c_char_p
     for f in (L.tp_project_3d_to_2d, L.tp_project_2d_to_2d, L.tp_backproject_2d_to_3d,
               L.tp_backproject_2d_to_2d, L.tp_project_backward, L.tp_backproject_backward,
-              L.tp_pad_volume, L.tp_crop_volume):
+              L.tp_pad_volume, L.tp_crop_volume, L.tp_project_3d_to_2d_ws,
+              L.tp_project_backward_ws):
         f.restype = I
     return L
 
@@ -73,7 +79,8 @@ def lib() -> ctypes.CDLL:
 def header_symbols() -> list[str]:
     """Names of the functions include/tp.h declares."""
     text = HEADER.read_text()
-    return sorted(set(re.findall(r"^\s*(?:tp_status|const char\*)\s+(tp_\w+)\s*\(", text, re.M)))
+    return sorted(set(re.findall(r"^\s*(?:tp_status|const char\*|size_t)\s+(tp_\w+)\s*\(", text,
+                                 re.M)))
 
 
 # ------------------------------------------------------------- marshalling ----
@@ -206,6 +213,44 @@ def tp_backproject_backward(ndim, proj, weights, rot, shift, grad_vol, grad_wvol
           "tp_backproject_backward")
 
 
+def tp_workspace_size(ndim, n_rec, Dv, opts=None) -> int:
+    return int(_LIB.tp_workspace_size(int(ndim), int(n_rec), int(Dv), _opts(opts)))
+
+
+def _ws(workspace):
+    if workspace is None:
+        return None, 0
+    if workspace.dtype != torch.uint8 or not workspace.is_cuda or not workspace.is_contiguous():
+        raise TypeError("workspace must be a contiguous CUDA uint8 tensor")
+    return ctypes.c_void_p(workspace.data_ptr()), workspace.numel()
+
+
+def tp_project_3d_to_2d_ws(vol, rot, shift, out, workspace, opts=None, stream=None):
+    _need(vol, torch.complex64, "vol", 4)
+    _need(out, torch.complex64, "out", 4)
+    n_rot, n_pose, n_sh = _rs(rot, shift, 3)
+    wp, wb = _ws(workspace)
+    _call(_LIB.tp_project_3d_to_2d_ws(_ptr(vol), vol.shape[0], vol.shape[1], _ptr(rot), n_rot,
+                                      n_pose, _ptr(shift), n_sh, _ptr(out), out.shape[2], wp, wb,
+                                      _opts(opts), _stream(stream)), "tp_project_3d_to_2d_ws")
+
+
+def tp_project_backward_ws(ndim, rec, rot, shift, grad_out, grad_rec, grad_rot, grad_shift,
+                           workspace, opts=None, stream=None):
+    _need(rec, torch.complex64, "rec", ndim + 1)
+    _need(grad_out, torch.complex64, "grad_out", 4)
+    _need(grad_rec, torch.complex64, "grad_rec", ndim + 1)
+    _need(grad_rot, torch.float32, "grad_rot", 4)
+    _need(grad_shift, torch.float32, "grad_shift", 3)
+    n_rot, n_pose, n_sh = _rs(rot, shift, ndim)
+    wp, wb = _ws(workspace)
+    _call(_LIB.tp_project_backward_ws(int(ndim), _ptr(rec), rec.shape[0], rec.shape[1], _ptr(rot),
+                                      n_rot, n_pose, _ptr(shift), n_sh, _ptr(grad_out),
+                                      grad_out.shape[2], _ptr(grad_rec), _ptr(grad_rot),
+                                      _ptr(grad_shift), wp, wb, _opts(opts), _stream(stream)),
+          "tp_project_backward_ws")
+
+
 def tp_pad_volume(ndim, vol, factor, out, stream=None):
     _need(vol, torch.float32, "vol", ndim + 1)
     _need(out, torch.float32, "out", ndim + 1)
@@ -293,3 +338,9 @@ def crop_volume(padded, D, factor, ndim=3, stream=None):
                       device=padded.device)
     tp_crop_volume(ndim, padded, factor, out, stream)
     return out
+
+
+def workspace_for(rec, opts=None):
+    """A workspace (CUDA uint8 tensor) for the 3D gathers over `rec`, or None when unused."""
+    n = tp_workspace_size(rec.dim() - 1, rec.shape[0], rec.shape[1], opts)
+    return torch.empty(n, dtype=torch.uint8, device=rec.device) if n else None

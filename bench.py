@@ -240,17 +240,20 @@ def run_ours(args, wl):
     gV = torch.empty_like(V)
     gR = torch.empty_like(R)
     gS = torch.empty((1 if S is None else S.shape[0], wl.n_pose, 2), device=dev)
+    # workspace of the gathers: each _ws call writes the grouped copy of the volume into it
+    # (one short kernel) before its gather
+    WS = tp.workspace_for(V, op)
 
     # The fused backward is issued as two C-ABI calls (pose gradients, then the volume
-    # gradient): the same outputs as one call, but each call is a single kernel, so CUDA
-    # events give every kernel's own duration.
+    # gradient): the same outputs as one call, but each call is one gather or one scatter,
+    # so CUDA events give every kernel's own duration.
     def step(ev=None):
         if ev is not None:
             ev[0].record(stream)
-        tp.tp_project_3d_to_2d(V, R, S, Y, op, stream)
+        tp.tp_project_3d_to_2d_ws(V, R, S, Y, WS, op, stream)
         if ev is not None:
             ev[1].record(stream)
-        tp.tp_project_backward(3, V, R, S, G, None, gR, gS, op, stream)
+        tp.tp_project_backward_ws(3, V, R, S, G, None, gR, gS, WS, op, stream)
         if ev is not None:
             ev[2].record(stream)
         tp.tp_project_backward(3, V, R, S, G, gV, None, None, op, stream)
@@ -312,8 +315,8 @@ def run_ours(args, wl):
             if dS is not None:
                 dS.copy_(hS, non_blocking=True)
             dG.copy_(hG, non_blocking=True)
-            tp.tp_project_3d_to_2d(dV, dR, dS, Y, op, stream)
-            tp.tp_project_backward(3, dV, dR, dS, dG, gV, gR, gS, op, stream)
+            tp.tp_project_3d_to_2d_ws(dV, dR, dS, Y, WS, op, stream)
+            tp.tp_project_backward_ws(3, dV, dR, dS, dG, gV, gR, gS, WS, op, stream)
             if world > 1:
                 dist.all_reduce(torch.view_as_real(gV))
             oY.copy_(Y, non_blocking=True)
@@ -390,7 +393,7 @@ def run_ours(args, wl):
             "data": "synthetic (seeded rfft of N(0,1) volume, uniform SO(3), CN(0,1) upstream grad)",
             "config": workload_config(wl, "inputs larger than L2 (1.09 GB upstream grad read and "
                                           "1.09 GB projections written per step); no flush"),
-            "gpu_launches": 3 * args.steps,
+            "gpu_launches": (3 + 2 * (WS is not None)) * args.steps,
             "kernel_ms": kms,
             "roofline": roofline, "roofline_onchip": onchip,
             "cpu_baseline": cpu, "e2e": e2e, "clocks": clocks,

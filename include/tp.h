@@ -59,6 +59,8 @@
 #ifndef TP_H
 #define TP_H
 
+#include <stddef.h>
+
 #ifdef __cplusplus
 extern "C" {
 #endif
@@ -135,6 +137,36 @@ tp_status tp_project_backward(int ndim, const void* rec, int n_rec, int Dv, cons
                               int n_rot, int n_pose, const float* shift, int n_sh,
                               const void* grad_out, int Do, void* grad_rec, float* grad_rot,
                               float* grad_shift, const tp_opts* opts, void* stream);
+
+/* Optional workspace of the 3D gathers.  tp_project_3d_to_2d_ws and tp_project_backward_ws
+ * are tp_project_3d_to_2d and tp_project_backward with a caller-owned device workspace; the
+ * results are the same (the same taps, weights and summation order).  The call first writes
+ * a grouped copy of the volumes into the workspace -- for every voxel the NT taps x .. x+NT-1
+ * of its row, NT = 4 (cubic) or 2 (linear), zeros past x = Dv/2, layout
+ * [n_rec][Dv][Dv][Dv/2+1][NT] complex -- and the gathers then read each row of taps with
+ * one aligned vector load instead of several unaligned ones.  It costs NT times the volumes'
+ * memory and one pass over them per call; it pays when many poses share the volumes.
+ * This is a B300 layout choice; the pages have no counterpart.
+ *
+ * tp_workspace_size returns the bytes needed (n_rec * Dv * Dv * (Dv/2+1) * NT * 8), or 0
+ * when the workspace would not be used (ndim = 2, invalid sizes or options, or NT times one
+ * volume's elements >= 2^31).  workspace = NULL, or a size of 0, runs the plain path.
+ * Errors, in addition to the plain call's: TP_ERR_SHAPE when workspace_bytes is below the
+ * size needed, TP_ERR_VALUE when the workspace is not 32-byte aligned.  The workspace must
+ * not overlap any argument; its contents are scratch (undefined after the call), and two
+ * calls in flight at once need two workspaces. */
+size_t tp_workspace_size(int ndim, int n_rec, int Dv, const tp_opts* opts);
+
+tp_status tp_project_3d_to_2d_ws(const void* vol, int n_rec, int Dv, const float* rot, int n_rot,
+                                 int n_pose, const float* shift, int n_sh, void* out, int Do,
+                                 void* workspace, size_t workspace_bytes, const tp_opts* opts,
+                                 void* stream);
+
+tp_status tp_project_backward_ws(int ndim, const void* rec, int n_rec, int Dv, const float* rot,
+                                 int n_rot, int n_pose, const float* shift, int n_sh,
+                                 const void* grad_out, int Do, void* grad_rec, float* grad_rot,
+                                 float* grad_shift, void* workspace, size_t workspace_bytes,
+                                 const tp_opts* opts, void* stream);
 
 /* Backward of tp_backproject_2d_to_3d (ndim = 3) or tp_backproject_2d_to_2d (ndim = 2): the
  * gradients of the back-projection itself, for upstream gradients grad_vol (complex,

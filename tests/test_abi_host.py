@@ -21,7 +21,8 @@ def test_header_symbols_are_exported():
     names = tp.header_symbols()
     assert set(names) == {"tp_project_3d_to_2d", "tp_backproject_2d_to_3d", "tp_project_2d_to_2d",
                           "tp_backproject_2d_to_2d", "tp_project_backward", "tp_backproject_backward",
-                          "tp_pad_volume", "tp_crop_volume", "tp_status_string"}
+                          "tp_pad_volume", "tp_crop_volume", "tp_status_string",
+                          "tp_workspace_size", "tp_project_3d_to_2d_ws", "tp_project_backward_ws"}
     for n in names:
         assert hasattr(L, n), n
     dyn = subprocess.run(["nm", "-D", "--defined-only", str(tp.LIB_PATH)], capture_output=True,
@@ -134,6 +135,30 @@ def test_pad_argument_errors(fn):
     assert f(3, FAKE, 1, 8, 2, None, None) == 1
     assert f(3, FAKE + 2, 1, 8, 2, FAKE, None) == 3
     assert f(3, None, 0, 8, 2, None, None) == 0
+
+
+def test_workspace_size():
+    assert tp.tp_workspace_size(3, 1, 128, tp.make_opts(1)) == 128 * 128 * 65 * 4 * 8
+    assert tp.tp_workspace_size(3, 2, 64, tp.make_opts(0)) == 2 * 64 * 64 * 33 * 2 * 8
+    assert tp.tp_workspace_size(2, 1, 128, tp.make_opts(1)) == 0      # 2D: not used
+    assert tp.tp_workspace_size(3, 1, 7, tp.make_opts(1)) == 0        # odd box
+    assert tp.tp_workspace_size(3, 1, 1024, tp.make_opts(1)) == 0     # 32-bit offsets
+    assert tp.tp_workspace_size(3, 1, 128, tp.make_opts(5)) == 0      # bad interp
+
+
+def test_workspace_argument_errors():
+    need = tp.tp_workspace_size(3, 1, 8, tp.make_opts())
+    pw = L.tp_project_3d_to_2d_ws
+    assert pw(FAKE, 1, 8, FAKE, 1, 2, None, 1, FAKE, 8, FAKE, need - 8, opts(), None) == 2
+    assert pw(FAKE, 1, 8, FAKE, 1, 2, None, 1, FAKE, 8, FAKE + 16, need, opts(), None) == 3
+    assert pw(FAKE, 1, 7, FAKE, 1, 2, None, 1, FAKE, 8, FAKE, need, opts(), None) == 2
+    assert pw(None, 1, 8, FAKE, 1, 2, None, 1, FAKE, 8, FAKE, need, opts(), None) == 1
+    bw = L.tp_project_backward_ws
+    assert bw(3, FAKE, 1, 8, FAKE, 1, 2, None, 1, FAKE, 8, None, FAKE, None, FAKE, 1, opts(), None) == 2
+    assert bw(3, FAKE, 1, 8, FAKE, 1, 2, None, 1, FAKE, 8, None, FAKE, None, FAKE + 8, need, opts(),
+              None) == 3
+    assert bw(3, None, 1, 8, FAKE, 1, 2, None, 1, FAKE, 8, None, FAKE, None, FAKE, need, opts(),
+              None) == 1
 
 
 def test_binding_rejects_bad_tensors():

@@ -116,6 +116,37 @@ def test_backproject_accumulate_and_skips(ndim):
     assert max_rel(host(vol), r_vol) <= TOL_BWD
 
 
+CASES3 = [c for c in CASES if c[0] == 3]
+
+
+@pytest.mark.parametrize("case", CASES3, ids=[str(c) for c in CASES3])
+def test_workspace_path(case):
+    """The gathers reading the grouped copy in a workspace give the plain call's forward bit
+    for bit (same taps, weights and order) and the oracle's gradients."""
+    ndim, Do = case[0], case[5]
+    rec, rot, shift, grad, _, kw, op = make_case(case, seed=7)
+    V, R, S, G = dev(rec), dev(rot), dev(shift), dev(grad)
+    ws = tp.workspace_for(V, op)
+    assert ws is not None and ws.numel() == tp.tp_workspace_size(3, rec.shape[0], rec.shape[1], op)
+    y0 = tp.project(V, R, S, Do=Do, opts=op)
+    y1 = torch.empty_like(y0)
+    tp.tp_project_3d_to_2d_ws(V, R, S, y1, ws, op)
+    assert torch.equal(y0, y1)
+    g_rot = torch.empty_like(R)
+    g_sh = torch.empty((1 if S is None else S.shape[0], R.shape[1], 2), device="cuda")
+    g_rec = torch.empty_like(V)
+    tp.tp_project_backward_ws(3, V, R, S, G, g_rec, g_rot, g_sh, ws, op)
+    r_rec, r_rot, r_sh = oracle.project_backward(ndim, rec, rot, grad, shift, **kw)
+    assert max_rel(host(g_rec), r_rec) <= TOL_BWD
+    assert max_rel(host(g_rot), r_rot) <= TOL_BWD
+    if shift is not None:
+        assert max_rel(host(g_sh), r_sh) <= TOL_BWD
+    # a NULL workspace is the plain path
+    y2 = torch.empty_like(y0)
+    tp.tp_project_3d_to_2d_ws(V, R, S, y2, None, op)
+    assert torch.equal(y0, y2)
+
+
 def _bp_grads(case, with_weights, seed):
     ndim = case[0]
     Gv, rot, shift, proj, w, kw, op = make_case(case, seed=seed)

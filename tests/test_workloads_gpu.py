@@ -105,8 +105,15 @@ def _fwdbwd3d_sampled(name, n_pix=6000, n_poses=48):
     V, R, S, G = dev(wl.rec), dev(wl.rot), dev(wl.shift), dev(wl.grad)
     op = wl_opts(wl)
     kw = oracle_kw(wl)
-    y = tp.project(V, R, S, opts=op)
-    g_rec, g_rot, g_sh = tp.project_backward(V, R, G, S, opts=op)
+    # the benchmark's calls: the gathers read the grouped copy in a workspace
+    ws = tp.workspace_for(V, op)
+    y = torch.empty_like(G)
+    tp.tp_project_3d_to_2d_ws(V, R, S, y, ws, op)
+    assert torch.equal(y, tp.project(V, R, S, opts=op))
+    g_rec, g_rot = torch.empty_like(V), torch.empty_like(R)
+    g_sh = torch.empty((S.shape[0], wl.n_pose, 2), device="cuda")
+    tp.tp_project_backward_ws(3, V, R, S, G, None, g_rot, g_sh, ws, op)
+    tp.tp_project_backward(3, V, R, S, G, g_rec, None, None, op)
     rng = np.random.default_rng(11)
     n_items = wl.n_rec * wl.n_pose
     items = rng.integers(0, n_items, n_pix)
