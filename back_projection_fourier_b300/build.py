@@ -15,7 +15,7 @@ PKG = Path(__file__).resolve().parent
 CSRC = PKG / "csrc"
 LIB = PKG / "libtp.so"
 INCLUDE = PKG.parent / "include"
-SOURCES = ["kernels.cu", "pad.cu", "tp_abi.cu"]
+SOURCES = ["kernels.cu", "pad.cu", "tp_abi.cu", "no_alloc.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 

@@ -57,6 +57,7 @@ def _load() -> ctypes.CDLL:
     L.tp_workspace_size.restype = Z
     L.tp_project_3d_to_2d_ws.argtypes = [P, I, I, P, I, I, P, I, P, I, P, Z, O, P]
     L.tp_project_backward_ws.argtypes = [I, P, I, I, P, I, I, P, I, P, I, P, P, P, P, Z, O, P]
+    L.tp_project_3d_to_2d_noalloc.argtypes = [P, I, I, P, I, I, P, I, P, I, O, P]
     L.tp_pad_volume.argtypes = [I, P, I, I, I, P, P]
     L.tp_crop_volume.argtypes = [I, P, I, I, I, P, P]
     L.tp_status_string.argtypes = [I]
@@ -64,7 +65,7 @@ def _load() -> ctypes.CDLL:
     for f in (L.tp_project_3d_to_2d, L.tp_project_2d_to_2d, L.tp_backproject_2d_to_3d,
               L.tp_backproject_2d_to_2d, L.tp_project_backward, L.tp_backproject_backward,
               L.tp_pad_volume, L.tp_crop_volume, L.tp_project_3d_to_2d_ws,
-              L.tp_project_backward_ws):
+              L.tp_project_backward_ws, L.tp_project_3d_to_2d_noalloc):
         f.restype = I
     return L
 
@@ -249,6 +250,16 @@ def tp_project_backward_ws(ndim, rec, rot, shift, grad_out, grad_rec, grad_rot, 
                                       grad_out.shape[2], _ptr(grad_rec), _ptr(grad_rot),
                                       _ptr(grad_shift), wp, wb, _opts(opts), _stream(stream)),
           "tp_project_backward_ws")
+
+
+def tp_project_3d_to_2d_noalloc(vol, rot, shift, out, opts=None, stream=None):
+    _need(vol, torch.complex64, "vol", 4)
+    _need(out, torch.complex64, "out", 4)
+    n_rot, n_pose, n_sh = _rs(rot, shift, 3)
+    _call(_LIB.tp_project_3d_to_2d_noalloc(_ptr(vol), vol.shape[0], vol.shape[1], _ptr(rot), n_rot,
+                                           n_pose, _ptr(shift), n_sh, _ptr(out), out.shape[2],
+                                           _opts(opts), _stream(stream)),
+          "tp_project_3d_to_2d_noalloc")
 
 
 def tp_pad_volume(ndim, vol, factor, out, stream=None):

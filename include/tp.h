@@ -168,6 +168,25 @@ tp_status tp_project_backward_ws(int ndim, const void* rec, int n_rec, int Dv, c
                                  float* grad_shift, void* workspace, size_t workspace_bytes,
                                  const tp_opts* opts, void* stream);
 
+/* tp_project_3d_to_2d with the workspace path, for callers that cannot allocate device
+ * memory and cannot pass a workspace: code whose device memory belongs entirely to another
+ * allocator (a framework's caching allocator, a fixed-budget memory pool) and code on a
+ * latency-critical path that must not call cudaMalloc, which can synchronise the device.
+ * The pages have no counterpart; this is a property of the library, not of the method.
+ *   Arguments, layouts and results as tp_project_3d_to_2d.  The grouped copy of the volumes
+ *   goes into a fixed scratch array of 34078720 bytes (one Dv = 128 volume with cubic taps)
+ *   that the library holds in device memory on every GPU that loads it, until the process
+ *   exits.  Sizes whose grouped copy needs more (tp_workspace_size above 34078720) return
+ *   TP_ERR_SHAPE before anything is enqueued.  The call allocates nothing.
+ *   The first call on a device looks up the array's device address (cudaGetSymbolAddress)
+ *   and keeps it; make that first call before any stream capture begins.
+ *   All calls share the one array and each overwrites what it reads, so calls whose work
+ *   overlaps on the GPU (other streams, other host threads) race and must be ordered by
+ *   the caller. */
+tp_status tp_project_3d_to_2d_noalloc(const void* vol, int n_rec, int Dv, const float* rot,
+                                      int n_rot, int n_pose, const float* shift, int n_sh,
+                                      void* out, int Do, const tp_opts* opts, void* stream);
+
 /* Backward of tp_backproject_2d_to_3d (ndim = 3) or tp_backproject_2d_to_2d (ndim = 2): the
  * gradients of the back-projection itself, for upstream gradients grad_vol (complex,
  * reconstruction-shaped) of the data volume and grad_wvol (fp32, reconstruction-shaped) of

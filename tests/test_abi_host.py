@@ -22,7 +22,8 @@ def test_header_symbols_are_exported():
     assert set(names) == {"tp_project_3d_to_2d", "tp_backproject_2d_to_3d", "tp_project_2d_to_2d",
                           "tp_backproject_2d_to_2d", "tp_project_backward", "tp_backproject_backward",
                           "tp_pad_volume", "tp_crop_volume", "tp_status_string",
-                          "tp_workspace_size", "tp_project_3d_to_2d_ws", "tp_project_backward_ws"}
+                          "tp_workspace_size", "tp_project_3d_to_2d_ws", "tp_project_backward_ws",
+                          "tp_project_3d_to_2d_noalloc"}
     for n in names:
         assert hasattr(L, n), n
     dyn = subprocess.run(["nm", "-D", "--defined-only", str(tp.LIB_PATH)], capture_output=True,
