@@ -854,6 +854,7 @@ __global__ void __launch_bounds__(kThreads) scatter_tile_kernel(
                   NWARP * (WTS ? kTileCap : 0) + warp * TR::WORDS;
     int* reci = reinterpret_cast<int*>(recf);
     static_assert(TR::WORDS % 4 == 0 && (kTileCap * 4) % 16 == 0, "16-byte aligned records");
+    static_assert(TR::WORDS >= kBoxRows, "the record space holds the flush's row table");
 
     __shared__ float Rs[9];
     __shared__ float2 sh;
@@ -1045,31 +1046,48 @@ __global__ void __launch_bounds__(kThreads) scatter_tile_kernel(
                     }
                     __syncwarp();
                 }
-                // ---- add the box to the volume (read and clear): the NX used columns of
-                // every box row; e / NX and r / NY by exact multiply-shift (e < 2^10, NX, NY <= 81)
+                // ---- add the box to the volume (read and clear).  The records are dead
+                // now: their space holds the global offset of every box row (-1 outside the
+                // band).  Entries e < NX * NY * NZ map to row r = e / NX and column e % NX by
+                // exact multiply-shift (e < 2^10, NX, NY <= 81); only non-zero entries are
+                // added and cleared.
                 if (boxed) {
-                    const int nused = NX * NY * NZ;
-                    const unsigned mx = (65536u + NX - 1) / NX, my = (65536u + NY - 1) / NY;
+                    const int nrows = NY * NZ;
+                    const unsigned my = (65536u + NY - 1) / NY;
+                    int* rowoff = reci;
+                    for (int r = lane; r < nrows; r += 32) {
+                        const int zi = (int)(((unsigned)r * my) >> 16);
+                        const int iy = full_index(y0 + r - zi * NY, g.Dv, g.halfv, g.centered);
+                        const int iz = full_index(z0 + zi, g.Dv, g.halfv, g.centered);
+                        rowoff[r] = (iy >= 0 && iz >= 0) ? (iz * g.Dv + iy) * g.Hv : -1;
+                    }
+                    __syncwarp();
+                    const unsigned mx = (65536u + NX - 1) / NX;
+                    const int nused = nrows * NX;
                     for (int e = lane; e < nused; e += 32) {
                         const int r = (int)(((unsigned)e * mx) >> 16);
                         const int xi = e - r * NX;
-                        const int zi = (int)(((unsigned)r * my) >> 16);
-                        const int yi = r - zi * NY;
-                        const int ux = x0 + xi;
-                        const int iy = full_index(y0 + yi, g.Dv, g.halfv, g.centered);
-                        const int iz = full_index(z0 + zi, g.Dv, g.halfv, g.centered);
-                        const bool ok = iy >= 0 && iz >= 0 && ux >= 0 && ux <= g.halfv;
-                        const long long off = ((long long)iz * g.Dv + iy) * g.Hv + ux;
                         const int be = r * kBoxPitch + xi;
+                        const int ux = x0 + xi;
+                        bool hit = false;
+                        float2 a = make_float2(0.f, 0.f);
+                        float b = 0.f;
                         if (DATA) {
-                            const float2 a = acc[be];
-                            if (ok && (a.x != 0.f || a.y != 0.f)) atomicAdd(G + off, a);
-                            acc[be] = make_float2(0.f, 0.f);
+                            a = acc[be];
+                            hit = a.x != 0.f || a.y != 0.f;
                         }
                         if (WTS) {
-                            const float b = wacc[be];
-                            if (ok && b != 0.f) atomicAdd(Wt + off, b);
-                            wacc[be] = 0.f;
+                            b = wacc[be];
+                            hit = hit || b != 0.f;
+                        }
+                        if (hit) {
+                            const int ro = rowoff[r];
+                            if (ro >= 0 && ux >= 0 && ux <= g.halfv) {
+                                if (DATA && (a.x != 0.f || a.y != 0.f)) atomicAdd(G + ro + ux, a);
+                                if (WTS && b != 0.f) atomicAdd(Wt + ro + ux, b);
+                            }
+                            if (DATA) acc[be] = make_float2(0.f, 0.f);
+                            if (WTS) wacc[be] = 0.f;
                         }
                     }
                 }

@@ -54,6 +54,8 @@ def parse():
     ap.add_argument("--cpu-sample", type=int, default=16384, help="poses in the oracle sample")
     ap.add_argument("--batch", type=int, default=None,
                     help="override the workload's batch (small cases for profiling only)")
+    ap.add_argument("--interp", choices=["linear", "cubic"], default=None,
+                    help="override the workload's interpolation (insertion: both are asked for)")
     ap.add_argument("--study", choices=["oversampling"], default=None,
                     help="instead of the step: time the on-the-fly oversampling comparison")
     ap.add_argument("--study-poses", default="1,16,256,4096,16384",
@@ -84,23 +86,48 @@ def kernel_hash() -> str:
 
 # ----------------------------------------------------------------- oracle ----
 
-def oracle_fwdbwd_rate(wl, n_poses: int, nthreads: int) -> tuple[float, str]:
-    """Projections/s of the fp64 oracle's forward + backward on the first n_poses poses of
-    every reconstruction."""
+def metric_for(wl) -> str:
+    """The headline metric for the headline workload; the same wording for the others."""
+    if wl.name == DEFAULT_WORKLOAD:
+        return METRIC
+    what = {"fwd": "forward", "insert": "insertion with weights", "fwdbwd": "fwd+bwd"}[wl.op]
+    if wl.ndim == 2:
+        what = "2D rotation " + what
+    recs = f", {wl.n_rec} reconstructions" if wl.ndim == 3 and wl.n_rec > 1 else ""
+    return f"projections/sec {what} at D={wl.D} {'cubic' if wl.interp else 'linear'}{recs}"
+
+
+def oracle_rate(wl, n_poses: int, nthreads: int) -> tuple[float, str]:
+    """Projections/s of the fp64 oracle on the workload's own operation, over the first
+    n_poses poses of every reconstruction (3D) or the first n_poses images (2D)."""
     import oracle
 
-    n = min(n_poses, wl.n_pose)
-    idx = np.arange(n)
-    take = lambda a: None if a is None else np.ascontiguousarray(a[:, idx])  # noqa: E731
     kw = dict(interp=wl.interp, layout=wl.layout, cutoff=wl.rc, nthreads=nthreads)
+    if wl.ndim == 3:
+        n = min(n_poses, wl.n_pose)
+        take = lambda a: None if a is None else np.ascontiguousarray(a[:, :n])  # noqa: E731
+        rec, items = wl.rec, wl.n_rec * n
+        per = f" of each of {wl.n_rec} reconstructions" if wl.n_rec > 1 else ""
+        what = f"first {n} of {wl.n_pose} poses{per}"
+    else:
+        n = min(n_poses, wl.n_rec)
+        take = lambda a: None if a is None else np.ascontiguousarray(a[:n])  # noqa: E731
+        rec, items = take(wl.rec), n
+        what = f"first {n} of {wl.n_rec} images"
     rot, sh, g = take(wl.rot), take(wl.shift), take(wl.grad)
     t0 = time.perf_counter()
-    oracle.project(wl.ndim, wl.rec, rot, sh, **kw)
-    oracle.project_backward(wl.ndim, wl.rec, rot, g, sh, **kw)
+    if wl.op == "insert":
+        w = take(np.ascontiguousarray(wl.weights))
+        oracle.backproject(wl.ndim, g, rot, weights=w, shift=sh, Dv=wl.D, **kw)
+        op = "insertion with weights"
+    else:
+        oracle.project(wl.ndim, rec, rot, sh, **kw)
+        op = "forward"
+        if wl.op == "fwdbwd":
+            oracle.project_backward(wl.ndim, rec, rot, g, sh, **kw)
+            op = "forward + full backward"
     dt = time.perf_counter() - t0
-    per = f" of each of {wl.n_rec} reconstructions" if wl.n_rec > 1 else ""
-    return wl.n_rec * n / dt, (f"first {n} of {wl.n_pose} poses{per}, forward + full backward, "
-                               f"fp64, {dt:.1f} s")
+    return items / dt, f"{what}, {op}, fp64, {dt:.1f} s"
 
 
 def run_reference(args, wl):
@@ -108,21 +135,22 @@ def run_reference(args, wl):
     if rank != 0:
         return 0
     nthreads = cores()
-    per_step = max(8, min(args.cpu_sample // 4 // wl.n_rec, wl.n_pose))
-    items = per_step * wl.n_rec
+    n_units = wl.n_pose if wl.ndim == 3 else wl.n_rec
+    per_step = max(8, min(args.cpu_sample // 4 // (wl.n_rec if wl.ndim == 3 else 1), n_units))
+    items = per_step * (wl.n_rec if wl.ndim == 3 else 1)
     import oracle
 
     oracle.build()
     for _ in range(args.warmup):
-        oracle_fwdbwd_rate(wl, per_step, nthreads)
+        oracle_rate(wl, per_step, nthreads)
     t0 = time.perf_counter()
     for _ in range(args.steps):
-        oracle_fwdbwd_rate(wl, per_step, nthreads)
+        oracle_rate(wl, per_step, nthreads)
     dt = time.perf_counter() - t0
     value = items * args.steps / dt
-    sample = f"{items} of {wl.B} projections per step (forward + full backward, fp64)"
+    sample = f"{items} of {wl.B} projections per step ({wl.op}, fp64)"
     line = {
-        "impl": "reference", "metric": METRIC, "value": value, "unit": "projections/s",
+        "impl": "reference", "metric": metric_for(wl), "value": value, "unit": "projections/s",
         "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": 1e3 * dt / args.steps * (wl.B / items),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
@@ -262,6 +290,14 @@ def run_ours(args, wl):
         if world > 1:
             dist.all_reduce(torch.view_as_real(gV))
 
+    # inputs smaller than twice the 126 MB L2 get a 256 MB write between timed steps
+    step_bytes = 2 * G.numel() * 8 + V.numel() * 8
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev) if step_bytes < (256 << 20) else None
+    l2_note = ("L2 flushed between steps (256 MB write; step time = sum of the calls' events)"
+               if flush is not None else
+               f"inputs larger than L2 ({G.numel() * 8 / 1e9:.2f} GB upstream grad read and "
+               f"{G.numel() * 8 / 1e9:.2f} GB projections written per step); no flush")
+
     for _ in range(args.warmup):
         step()
     torch.cuda.synchronize()
@@ -280,6 +316,8 @@ def run_ours(args, wl):
     torch.cuda.synchronize()
     start.record(stream)
     for k in range(args.steps):
+        if flush is not None:
+            flush.zero_()
         step(evs[k])
     end.record(stream)
     torch.cuda.synchronize()
@@ -294,7 +332,12 @@ def run_ours(args, wl):
     kms = {"forward": statistics.mean(e[0].elapsed_time(e[1]) for e in evs),
            "grad_pose": statistics.mean(e[1].elapsed_time(e[2]) for e in evs),
            "grad_volume": statistics.mean(e[2].elapsed_time(e[3]) for e in evs)}
-    ms_step = ms / args.steps
+    # with an L2 flush between steps the step time is the sum of the calls' own events
+    ms_step = ms / args.steps if flush is None else sum(kms.values())
+    if flush is not None and world > 1:
+        t = torch.tensor([ms_step], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms_step = float(t.item())
     value = wl.B * world / (ms_step * 1e-3)
 
     # e2e: host (pinned) inputs -> device -> forward + backward -> host outputs, every step
@@ -381,18 +424,17 @@ def run_ours(args, wl):
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        rate, sample = oracle_fwdbwd_rate(wl, args.cpu_sample, cores())
+        rate, sample = oracle_rate(wl, args.cpu_sample, cores())
         cpu = {"value": rate, "unit": "projections/s", "cores": cores(), "kind": "oracle",
                "sample": sample}
 
     if rank == 0:
         line = {
-            "metric": METRIC, "value": value, "unit": "projections/s", "n_gpus": world,
+            "metric": metric_for(wl), "value": value, "unit": "projections/s", "n_gpus": world,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_step,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
             "data": "synthetic (seeded rfft of N(0,1) volume, uniform SO(3), CN(0,1) upstream grad)",
-            "config": workload_config(wl, "inputs larger than L2 (1.09 GB upstream grad read and "
-                                          "1.09 GB projections written per step); no flush"),
+            "config": workload_config(wl, l2_note),
             "gpu_launches": (3 + 2 * (WS is not None)) * args.steps,
             "kernel_ms": kms,
             "roofline": roofline, "roofline_onchip": onchip,
@@ -401,6 +443,99 @@ def run_ours(args, wl):
         print(json.dumps(line), flush=True)
     if world > 1:
         dist.destroy_process_group()
+    return 0
+
+
+def run_workload(args, wl):
+    """One GPU, any other workload: the forward-only 3D workload, the insertion (with its
+    CTF-like weights) and the 2D rotation workload (forward + backward).  Each C-ABI call of
+    the step is timed with CUDA events on the launch stream; inputs smaller than L2 are
+    followed, between steps, by a 256 MB write that flushes L2 (outside the timed calls)."""
+    import torch
+    from back_projection_fourier_b300 import tp
+
+    world, _, local = dist_env()
+    if world > 1:
+        raise SystemExit("the non-headline workloads run on one GPU")
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    stream = torch.cuda.current_stream(dev)
+    op = tp.make_opts(wl.interp, wl.layout, 1.0, wl.rc)
+    up = lambda a: None if a is None else torch.from_numpy(np.ascontiguousarray(a)).to(dev)  # noqa: E731
+    R, S = up(wl.rot), up(wl.shift)
+    img = wl.D * wl.H * 8
+    n_img = wl.n_rec * wl.n_pose
+    calls, launches = {}, 0
+    if wl.op == "fwd":
+        V = up(wl.rec)
+        Y = torch.empty((wl.n_rec, wl.n_pose, wl.D, wl.H), dtype=torch.complex64, device=dev)
+        WS = tp.workspace_for(V, op)
+        calls["forward"] = lambda: tp.tp_project_3d_to_2d_ws(V, R, S, Y, WS, op, stream)
+        launches = 1 + (WS is not None)
+        hbm = {"forward": n_img * img + V.numel() * 8}
+        what = "forward"
+    elif wl.op == "insert":
+        P, W = up(wl.grad), up(np.ascontiguousarray(wl.weights))
+        vol = torch.empty((1, wl.D, wl.D, wl.H), dtype=torch.complex64, device=dev)
+        wvol = torch.empty((1, wl.D, wl.D, wl.H), device=dev)
+        calls["insertion"] = lambda: tp.tp_backproject_2d_to_3d(P, W, R, S, vol, wvol, wl.D, False,
+                                                                op, stream)
+        launches = 1
+        hbm = {"insertion": n_img * (img + img // 2) + vol.numel() * 12}
+        what = "insertion with weights"
+    elif wl.op == "fwdbwd" and wl.ndim == 2:
+        V, G = up(wl.rec), up(wl.grad)
+        Y, gV, gR = torch.empty_like(G), torch.empty_like(V), torch.empty_like(R)
+        gS = torch.empty((S.shape[0], wl.n_pose, 2), device=dev)
+        calls["forward"] = lambda: tp.tp_project_2d_to_2d(V, R, S, Y, op, stream)
+        calls["grad_pose"] = lambda: tp.tp_project_backward(2, V, R, S, G, None, gR, gS, op, stream)
+        calls["grad_image"] = lambda: tp.tp_project_backward(2, V, R, S, G, gV, None, None, op,
+                                                             stream)
+        launches = 3
+        hbm = {"forward": 2 * n_img * img, "grad_pose": 2 * n_img * img,
+               "grad_image": 2 * n_img * img}
+        what = "2D rotation forward + backward"
+    else:
+        raise SystemExit(f"no timing recipe for workload {wl.name}")
+    step_bytes = sum(hbm.values())
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev) if step_bytes < (256 << 20) else None
+    names = list(calls)
+    ev = {k: (torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for k in names}
+    tot = {k: 0.0 for k in names}
+    for it in range(args.warmup + args.steps):
+        if flush is not None:
+            flush.zero_()
+        for k in names:
+            ev[k][0].record(stream)
+            calls[k]()
+            ev[k][1].record(stream)
+        torch.cuda.synchronize()
+        if it >= args.warmup:
+            for k in names:
+                tot[k] += ev[k][0].elapsed_time(ev[k][1])
+    kms = {k: v / args.steps for k, v in tot.items()}
+    ms_step = sum(kms.values())
+    dom = max(kms, key=kms.get)
+    peaks = {}
+    try:
+        peaks = json.loads((ROOT / "MEASURED_PEAKS.json").read_text())
+    except (OSError, ValueError):
+        pass
+    peak = float(peaks.get("hbm_gbs") or 6400.0)
+    achieved = hbm[dom] / (kms[dom] * 1e-3) / 1e9
+    line = {
+        "metric": metric_for(wl), "value": n_img / (ms_step * 1e-3),
+        "unit": "projections/s", "n_gpus": 1, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "f32", "data": "synthetic",
+        "config": dict(workload_config(wl, "L2 flushed between steps (256 MB write)" if flush is not None
+                                       else "inputs larger than L2; no flush"), step=what),
+        "gpu_launches": launches * args.steps, "kernel_ms": kms,
+        "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
+                     "frac": achieved / peak, "traffic": None, "kernel": dom,
+                     "peak_source": "measured" if peaks.get("hbm_gbs") else "fallback"},
+    }
+    print(json.dumps(line), flush=True)
     return 0
 
 
@@ -493,10 +628,12 @@ def main():
         world, rank, _ = dist_env()
         if rank != 0:
             return 0
-        return run_reference(args, synth.make_workload(args.workload))
-    wl = synth.make_workload(args.workload, B=args.batch)
+        interp = None if args.interp is None else (1 if args.interp == "cubic" else 0)
+        return run_reference(args, synth.make_workload(args.workload, interp=interp))
+    interp = None if args.interp is None else (1 if args.interp == "cubic" else 0)
+    wl = synth.make_workload(args.workload, B=args.batch, interp=interp)
     if wl.op != "fwdbwd" or wl.ndim != 3:
-        raise SystemExit("bench.py times the 3D forward + backward workloads")
+        return run_workload(args, wl)
     return run_ours(args, wl)
 
 
