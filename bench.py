@@ -54,6 +54,8 @@ def parse():
     ap.add_argument("--cpu-sample", type=int, default=16384, help="poses in the oracle sample")
     ap.add_argument("--batch", type=int, default=None,
                     help="override the workload's batch (small cases for profiling only)")
+    ap.add_argument("--e2e-chunks", type=int, default=8,
+                    help="pose chunks of the pipelined end-to-end step (copies overlap kernels)")
     ap.add_argument("--interp", choices=["linear", "cubic"], default=None,
                     help="override the workload's interpolation (insertion: both are asked for)")
     ap.add_argument("--study", choices=["oversampling"], default=None,
@@ -352,20 +354,53 @@ def run_ours(args, wl):
         dV, dR, dG = torch.empty_like(V), torch.empty_like(R), torch.empty_like(G)
         dS = torch.empty_like(S) if S is not None else None
 
+        # Pipelined over chunks of poses on three streams: the host->device copy of chunk c+1
+        # and the device->host copy of chunk c-1 overlap the kernels of chunk c.  Per chunk:
+        # forward, pose gradients, and the chunk's share of the volume gradient, accumulated
+        # by the insertion call (the transpose of the projection, the same kernel as the
+        # backward's volume gradient).  One reconstruction: chunks are contiguous pose ranges.
+        n_chunk = args.e2e_chunks if wl.n_rec == 1 else 1
+        bounds = [(wl.n_pose * c // n_chunk, wl.n_pose * (c + 1) // n_chunk) for c in range(n_chunk)]
+        s_in, s_out = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
+        ev_v = torch.cuda.Event()
+        ev_in = [torch.cuda.Event() for _ in bounds]
+        ev_done = [torch.cuda.Event() for _ in bounds]
+        ev_vol = torch.cuda.Event()
+        sl = lambda t, a, b: None if t is None else t[:, a:b]  # noqa: E731
+
         def e2e_step():
-            dV.copy_(hV, non_blocking=True)
-            dR.copy_(hR, non_blocking=True)
-            if dS is not None:
-                dS.copy_(hS, non_blocking=True)
-            dG.copy_(hG, non_blocking=True)
-            tp.tp_project_3d_to_2d_ws(dV, dR, dS, Y, WS, op, stream)
-            tp.tp_project_backward_ws(3, dV, dR, dS, dG, gV, gR, gS, WS, op, stream)
+            with torch.cuda.stream(s_in):
+                dV.copy_(hV, non_blocking=True)
+                dR.copy_(hR, non_blocking=True)
+                if dS is not None:
+                    dS.copy_(hS, non_blocking=True)
+                ev_v.record(s_in)
+                for c, (a, b) in enumerate(bounds):
+                    dG[:, a:b].copy_(hG[:, a:b], non_blocking=True)
+                    ev_in[c].record(s_in)
+            stream.wait_event(ev_v)
+            for c, (a, b) in enumerate(bounds):
+                stream.wait_event(ev_in[c])
+                Rc, Sc, Gc = sl(dR, a, b), sl(dS, a, b), sl(dG, a, b)
+                tp.tp_project_3d_to_2d_ws(dV, Rc, Sc, Y[:, a:b], WS, op, stream)
+                tp.tp_project_backward_ws(3, dV, Rc, Sc, Gc, None, gR[:, a:b], gS[:, a:b], WS, op,
+                                          stream)
+                tp.tp_backproject_2d_to_3d(Gc, None, Rc, Sc, gV, None, wl.D, c > 0, op, stream)
+                ev_done[c].record(stream)
             if world > 1:
                 dist.all_reduce(torch.view_as_real(gV))
-            oY.copy_(Y, non_blocking=True)
-            ogV.copy_(gV, non_blocking=True)
-            ogR.copy_(gR, non_blocking=True)
-            ogS.copy_(gS, non_blocking=True)
+            ev_vol.record(stream)
+            with torch.cuda.stream(s_out):
+                for c, (a, b) in enumerate(bounds):
+                    s_out.wait_event(ev_done[c])
+                    oY[:, a:b].copy_(Y[:, a:b], non_blocking=True)
+                    ogR[:, a:b].copy_(gR[:, a:b], non_blocking=True)
+                    ogS[:, a:b].copy_(gS[:, a:b], non_blocking=True)
+                s_out.wait_event(ev_vol)
+                ogV.copy_(gV, non_blocking=True)
+            # the next step's copies into the device inputs wait for this step's kernels
+            s_in.wait_stream(stream)
+            stream.wait_stream(s_out)
 
         for _ in range(max(1, args.warmup)):
             e2e_step()

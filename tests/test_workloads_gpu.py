@@ -148,3 +148,16 @@ def test_fwdbwd3d_d128_cubic_r8_full_sampled():
 
 def test_fwdbwd3d_d256_cubic_full_sampled():
     _fwdbwd3d_sampled("fwdbwd3d_d256_cubic_b50000", n_pix=4000, n_poses=24)
+
+
+def test_chunked_volume_gradient_equals_the_backward():
+    """The pipelined end-to-end step sums each pose chunk's volume gradient with the insertion
+    call (accumulate = 1): the same transpose as the backward's volume gradient."""
+    wl = synth.make_workload("fwdbwd3d_d128_cubic_b16384", B=1000)
+    V, R, S, G = dev(wl.rec), dev(wl.rot), dev(wl.shift), dev(wl.grad)
+    op = wl_opts(wl)
+    g_rec, _, _ = tp.project_backward(V, R, G, S, want_rot=False, want_shift=False, opts=op)
+    acc = torch.empty_like(V)
+    for c, (a, b) in enumerate([(0, 300), (300, 301), (301, 1000)]):
+        tp.tp_backproject_2d_to_3d(G[:, a:b], None, R[:, a:b], S[:, a:b], acc, None, wl.D, c > 0, op)
+    assert max_rel(host(acc), host(g_rec)) <= TOL_BWD
