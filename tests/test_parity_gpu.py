@@ -22,6 +22,8 @@ CASES = [
     (3, 0, 0, 1.5, 24, 16, -1.0, False, 2, 1, 11),
     (3, 1, 1, 2.0, 32, 16, 100.0, True, 1, 1, 9),
     (3, 1, 1, 1.0, 2, 2, -1.0, True, 1, 1, 5),
+    (3, 1, 0, 1.0, 30, 30, -1.0, True, 2, 2, 7),
+    (3, 0, 1, 1.25, 40, 32, 12.0, True, 3, 1, 6),
     (2, 1, 1, 1.0, 48, 48, -1.0, True, 5, 5, 3),
     (2, 0, 0, 1.0, 30, 30, -1.0, True, 3, 1, 4),
     (2, 1, 0, 1.5, 36, 24, 10.0, False, 4, 4, 2),
