@@ -30,7 +30,9 @@ namespace tp {
 namespace {
 
 constexpr int kThreads = 256;
-constexpr int kQueue = 2 * kThreads;
+// The pose-gradient gather runs in CTAs of 128 threads: at its 128 registers per thread that
+// is 4 CTAs per SM (4 items in flight) instead of 2, with cheaper per-item reductions.
+constexpr int kPoseThreads = 128;
 constexpr int kMaxTableRows = 4096;  // image boxes up to this size use the kept-pixel table
 
 struct ItemRange {
@@ -68,10 +70,11 @@ __device__ __forceinline__ int row_kept(const Geom& g, int i)
     return (k < g.halfo ? k : g.halfo) + 1;
 }
 
-// rowstart[i] = kept pixels in rows < i, for i = 0..Do (exclusive block scan).
+// rowstart[i] = kept pixels in rows < i, for i = 0..Do (exclusive scan over a CTA of BT).
+template <int BT = kThreads>
 __device__ void build_rowstart(const Geom& g, int* rowstart, int* scratch)
 {
-    const int per = (g.Do + kThreads - 1) / kThreads;
+    const int per = (g.Do + BT - 1) / BT;
     const int i0 = threadIdx.x * per;
     int sum = 0;
     for (int k = 0; k < per; ++k)
@@ -88,7 +91,7 @@ __device__ void build_rowstart(const Geom& g, int* rowstart, int* scratch)
     __syncthreads();
     if (threadIdx.x == 0) {
         int acc = 0;
-        for (int w = 0; w < kThreads / 32; ++w) {
+        for (int w = 0; w < BT / 32; ++w) {
             const int t = scratch[w];
             scratch[w] = acc;
             acc += t;
@@ -101,13 +104,13 @@ __device__ void build_rowstart(const Geom& g, int* rowstart, int* scratch)
             rowstart[i0 + k] = run;
             run += row_kept(g, i0 + k);
         }
-    if (threadIdx.x == kThreads - 1) rowstart[g.Do] = run;
+    if (threadIdx.x == BT - 1) rowstart[g.Do] = run;
     __syncthreads();
 }
 
 // Slow-path queue: pixels packed as (row << 16) | kx.
 struct Queue {
-    int* slots;  // [kQueue]
+    int* slots;  // [2 * threads of the CTA]
     int* count;  // shared counter
 };
 
@@ -122,7 +125,8 @@ __device__ __forceinline__ void enqueue(Queue q, bool slow, int row, int kx)
     if (slow) q.slots[base + __popc(mask & ((1u << lane) - 1))] = (row << 16) | kx;
 }
 
-// Sum of a per-thread value over the CTA, valid in thread 0.
+// Sum of a per-thread value over the CTA of BT threads, valid in thread 0.
+template <int BT = kThreads>
 __device__ __forceinline__ float block_sum(float v, float* red)
 {
 #pragma unroll
@@ -133,14 +137,15 @@ __device__ __forceinline__ float block_sum(float v, float* red)
     __syncthreads();
     float s = 0.f;
     if (threadIdx.x == 0)
-        for (int k = 0; k < kThreads / 32; ++k) s += red[k];
+        for (int k = 0; k < BT / 32; ++k) s += red[k];
     return s;
 }
 
 // Work split of one item's kept pixels over `splits` CTAs: chunks of whole CTA rounds.
+template <int BT = kThreads>
 __device__ __forceinline__ int kept_chunk(int nkept, int splits)
 {
-    return ((nkept + splits - 1) / splits + kThreads - 1) / kThreads * kThreads;
+    return ((nkept + splits - 1) / splits + BT - 1) / BT * BT;
 }
 
 // Image row holding kept pixel n0: the largest row r < Do with rowstart[r] <= n0.
@@ -200,7 +205,7 @@ __global__ void __launch_bounds__(kThreads, 3) project_kernel(
 {
     extern __shared__ int smem[];
     int* rowstart = smem;                    // [Do + 1]
-    int* qslots = smem + g.Do + 1;           // [kQueue]
+    int* qslots = smem + g.Do + 1;           // [2 * kThreads]
     __shared__ int scratch[kThreads / 32];
     __shared__ int qcount;
     build_rowstart(g, rowstart, scratch);
@@ -326,7 +331,7 @@ __device__ __forceinline__ void accumulate_grad(float* acc, float2 gp, float2 v,
 }
 
 template <int NDIM, int INTERP, int WIN>
-__global__ void __launch_bounds__(kThreads) grad_pose_kernel(
+__global__ void __launch_bounds__(kPoseThreads, 4) grad_pose_kernel(
     const float2* __restrict__ rec, const float* __restrict__ rot,
     const float* __restrict__ shift, const float2* __restrict__ gout,
     float* __restrict__ grot, float* __restrict__ gsh, Geom g, int splits, long long n_work,
@@ -336,15 +341,15 @@ __global__ void __launch_bounds__(kThreads) grad_pose_kernel(
     extern __shared__ int smem[];
     int* rowstart = smem;
     int* qslots = smem + g.Do + 1;
-    __shared__ int scratch[kThreads / 32];
-    __shared__ float red[kThreads / 32];
+    __shared__ int scratch[kPoseThreads / 32];
+    __shared__ float red[kPoseThreads / 32];
     __shared__ int qcount;
-    build_rowstart(g, rowstart, scratch);
+    build_rowstart<kPoseThreads>(g, rowstart, scratch);
     if (threadIdx.x == 0) qcount = 0;
     __syncthreads();
     const Queue q{qslots, &qcount};
     const int nkept = rowstart[g.Do];
-    const int chunk = kept_chunk(nkept, splits);
+    const int chunk = kept_chunk<kPoseThreads>(nkept, splits);
 
     // work unit = (item, part): part sums one chunk of the item's kept pixels
     for (long long w = blockIdx.x; w < n_work; w += gridDim.x) {
@@ -366,7 +371,7 @@ __global__ void __launch_bounds__(kThreads) grad_pose_kernel(
         };
         const int b0 = ir.part * chunk, b1 = min(nkept, b0 + chunk);
         int row = b0 < nkept ? row_of_kept(rowstart, g.Do, b0) : 0;
-        for (int base = b0; base < b1; base += kThreads) {
+        for (int base = b0; base < b1; base += kPoseThreads) {
             const int n = base + threadIdx.x;
             bool slow = false;
             int kx = 0;
@@ -382,15 +387,15 @@ __global__ void __launch_bounds__(kThreads) grad_pose_kernel(
             }
             enqueue(q, slow, row, kx);
             __syncthreads();
-            if (qcount >= kThreads) {
-                const int e = q.slots[qcount - kThreads + threadIdx.x];
+            if (qcount >= kPoseThreads) {
+                const int e = q.slots[qcount - kPoseThreads + threadIdx.x];
                 const int qrow = e >> 16, qkx = e & 0xffff;
                 float2 v, dv[3];
                 eval_general<NDIM, INTERP, true>(g, V, ip.R, qkx,
                                                  row_freq(qrow, g.Do, g.halfo, g.centered), v, dv);
                 add(qrow, qkx, v, dv);
                 __syncthreads();
-                if (threadIdx.x == 0) qcount -= kThreads;
+                if (threadIdx.x == 0) qcount -= kPoseThreads;
                 __syncthreads();
             }
         }
@@ -410,7 +415,7 @@ __global__ void __launch_bounds__(kThreads) grad_pose_kernel(
         const float two_pi_over_Do = 6.283185307179586f * g.inv_Do;
 #pragma unroll
         for (int k = 0; k < NG; ++k) {
-            const float s = block_sum(acc[k], red);
+            const float s = block_sum<kPoseThreads>(acc[k], red);
             if (threadIdx.x == 0) {
                 if (k < 2 * NDIM) {
                     if (grot) atomicAdd(grot + ri * NDIM * NDIM + (k / 2) * NDIM + (k % 2), g.o * s);
@@ -1212,16 +1217,16 @@ struct TableShape {
     long long n_work;
 };
 
-TableShape table_shape(const Geom& g, int sms, int ctas_per_sm)
+TableShape table_shape(const Geom& g, int sms, int ctas_per_sm, int threads = kThreads)
 {
     const long long n_items = (long long)g.n_rec * g.n_pose;
-    const long long max_parts = (g.img_elems + kThreads - 1) / kThreads;
+    const long long max_parts = (g.img_elems + threads - 1) / threads;
     TableShape t;
     t.splits = (int)item_splits(n_items, (long long)ctas_per_sm * sms, max_parts);
     t.n_work = n_items * t.splits;
     const long long cap = 16LL * sms;  // persistent-style: the table is built once per CTA
     t.grid = (unsigned)(t.n_work < cap ? t.n_work : cap);
-    t.smem = (size_t)(g.Do + 1 + kQueue) * sizeof(int);
+    t.smem = (size_t)(g.Do + 1 + 2 * threads) * sizeof(int);  // kept-pixel table + slow queue
     return t;
 }
 
@@ -1265,8 +1270,8 @@ void launch_grad_table(const Geom& g, const float2* R, const float* rot, const f
                        const float2* G, float* grot, float* gsh, const float2* grouped, int sms,
                        cudaStream_t stream)
 {
-    const TableShape t = table_shape(g, sms, 2);
-    grad_pose_kernel<NDIM, INTERP, WIN><<<t.grid, kThreads, t.smem, stream>>>(
+    const TableShape t = table_shape(g, sms, 4, kPoseThreads);
+    grad_pose_kernel<NDIM, INTERP, WIN><<<t.grid, kPoseThreads, t.smem, stream>>>(
         R, rot, shift, G, grot, gsh, g, t.splits, t.n_work, grouped);
 }
 
