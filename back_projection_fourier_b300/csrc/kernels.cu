@@ -198,7 +198,7 @@ __device__ __forceinline__ bool eval_fast(const Geom& g, const float2* __restric
 // ------------------------------------------------------------------ forward ----
 
 template <int NDIM, int INTERP, int WIN>
-__global__ void __launch_bounds__(kThreads, 3) project_kernel(
+__global__ void __launch_bounds__(kThreads, NDIM == 3 ? 3 : 4) project_kernel(
     const float2* __restrict__ rec, const float* __restrict__ rot,
     const float* __restrict__ shift, float2* __restrict__ out, Geom g, int splits, long long n_work,
     const float2* __restrict__ grouped)
@@ -1240,7 +1240,8 @@ template <int NDIM, int INTERP, int WIN>
 void launch_project_table(const Geom& g, const float2* R, const float* rot, const float* shift,
                           float2* Y, const float2* grouped, int sms, cudaStream_t stream)
 {
-    const TableShape t = table_shape(g, sms, 3);
+    // 3 resident CTAs per SM leave each 3D projection more L1; 2D images prefer 4
+    const TableShape t = table_shape(g, sms, NDIM == 3 ? 3 : 4);
     project_kernel<NDIM, INTERP, WIN><<<t.grid, kThreads, t.smem, stream>>>(
         R, rot, shift, Y, g, t.splits, t.n_work, grouped);
 }
