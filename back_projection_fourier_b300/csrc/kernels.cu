@@ -848,6 +848,7 @@ __global__ void __launch_bounds__(kThreads) scatter_tile_kernel(
     constexpr int T = NT * NT * NT;        // taps per pixel
     constexpr int LPP = T < 32 ? T : 32;   // lanes per pixel
     constexpr int TPL = T / LPP;           // taps per lane
+    static_assert(TPL == 1 || (NT == 4 && LPP == 32), "paired taps are z planes a and a + 2");
     constexpr int NWARP = kThreads / 32;
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     extern __shared__ __align__(16) unsigned char sm_raw[];
@@ -964,10 +965,21 @@ __global__ void __launch_bounds__(kThreads) scatter_tile_kernel(
                     weights<INTERP>(ez - flz, wz_);
                     float* rf = recf + lane * TR::STRIDE;
                     int* ri = reci + lane * TR::STRIDE;
+                    if constexpr (TPL == 2) {
+                        // a lane's two taps are z planes a and a + 2 of one y row: store them
+                        // as an adjacent pair, read back with one 8-byte load
 #pragma unroll
-                    for (int a = 0; a < NT; ++a)
+                        for (int a = 0; a < NT / 2; ++a)
 #pragma unroll
-                        for (int b = 0; b < NT; ++b) rf[TR::WZY + a * NT + b] = wz_[a] * wy_[b];
+                            for (int b = 0; b < NT; ++b)
+                                *reinterpret_cast<float2*>(rf + TR::WZY + 2 * (a * NT + b)) =
+                                    make_float2(wz_[a] * wy_[b], wz_[a + 2] * wy_[b]);
+                    } else {
+#pragma unroll
+                        for (int a = 0; a < NT; ++a)
+#pragma unroll
+                            for (int b = 0; b < NT; ++b) rf[TR::WZY + a * NT + b] = wz_[a] * wy_[b];
+                    }
 #pragma unroll
                     for (int k = 0; k < NT; ++k) rf[TR::WX + k] = wx_[k];
                     rf[TR::WT] = wt;
@@ -996,10 +1008,18 @@ __global__ void __launch_bounds__(kThreads) scatter_tile_kernel(
                         const float wxk = rf[TR::WX + tk];
                         const int rb = __float_as_int(head.w);
                         const int base = rb < 0 ? ~rb : rb;
+                        float wzy[TPL];
+                        if constexpr (TPL == 2) {
+                            const float2 pr = *reinterpret_cast<const float2*>(rf + TR::WZY + 2 * (ta[0] * NT + tb[0]));
+                            wzy[0] = pr.x;
+                            wzy[1] = pr.y;
+                        } else {
+                            wzy[0] = rf[TR::WZY + ta[0] * NT + tb[0]];
+                        }
                         if (rb >= 0) {
 #pragma unroll
                             for (int m = 0; m < TPL; ++m) {
-                                const float w = rf[TR::WZY + ta[m] * NT + tb[m]] * wxk;
+                                const float w = wzy[m] * wxk;
                                 const int e = base + toff[m];
                                 if (DATA) {
                                     float2 a = acc[e];
@@ -1016,7 +1036,7 @@ __global__ void __launch_bounds__(kThreads) scatter_tile_kernel(
                             const int pfz = ri[TR::FZ];
 #pragma unroll
                             for (int m = 0; m < TPL; ++m) {
-                                const float w = rf[TR::WZY + ta[m] * NT + tb[m]] * wxk;
+                                const float w = wzy[m] * wxk;
                                 const int ux = pfx + FIRST + tk;
                                 const bool direct = ux >= 1 || (ux == 0 && pass == 0);
                                 if (direct && boxed) {
