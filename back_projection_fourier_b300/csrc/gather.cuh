@@ -26,14 +26,6 @@ namespace tp {
 
 constexpr int kGrouped = 8;  // WIN tag of the grouped-row reader
 
-template <int WIN>
-struct Window;
-
-template <>
-struct Window<1> {
-    static constexpr int E = 0;  // unused
-};
-
 __device__ __forceinline__ float4 ldg_v4(const float2* p)
 {
     return __ldg(reinterpret_cast<const float4*>(p));

@@ -6,15 +6,17 @@
 // (accumulation into a 2D reconstruction); gradients for inputs, rotations and shifts
 // without stored intermediates (differentiation bullet); shifts by phase modulation.
 //
-// Gather kernels (forward projection; rotation / shift gradients).  A CTA owns one item
-// (reconstruction r, pose p) at a time (grid-stride over items) and stages the item's
-// rotation and shift.  Threads walk only the kept pixels (kx^2 + ky^2 <= rc^2) through a
-// per-CTA table of row offsets, in row-major order, so image reads and writes stay
-// coalesced.  Pixels whose taps are all read directly (the vast majority, see gather.cuh)
-// take the fast path; the others -- taps on the x = 0 plane or past x = Dv/2 -- are queued
-// in shared memory and evaluated densely with the exact per-tap rule, so they do not make
-// whole warps diverge.  The volume is read through the read-only path and stays
-// L2-resident (a D = 256 half volume is 68 MB of a 126 MB L2).
+// Gather kernels (forward projection; rotation / shift gradients).  A CTA owns one work
+// unit at a time (grid-stride): an item (reconstruction r, pose p), or a chunk of one item's
+// pixels when the batch has fewer items than resident CTAs.  Threads walk only the kept
+// pixels (kx^2 + ky^2 <= rc^2) through a per-CTA table of row offsets, in row-major order,
+// so image reads and writes stay coalesced.  Pixels whose taps are all read directly (the
+// vast majority, see gather.cuh) take the fast path, reading each row of taps either from
+// the volume in aligned vector windows or, with a workspace, from the grouped copy in one
+// aligned load; the others -- taps on the x = 0 plane or past x = Dv/2 -- are queued in
+// shared memory and evaluated densely with the exact per-tap rule, so they do not make whole
+// warps diverge.  The volume (and its grouped copy at D <= 128) stays L2-resident: a D = 256
+// half volume is 68 MB of a 126 MB L2.
 #include "gather.cuh"
 #include "kernels.h"
 #include "scatter.cuh"

@@ -80,9 +80,14 @@ def cores() -> int:
 
 
 def kernel_hash() -> str:
+    """Hash of the kernel sources without comments and blank lines: a counter capture stays
+    valid across comment edits and is dropped by any change to the code itself."""
     h = hashlib.sha256()
     for rel in KERNEL_SOURCES:
-        h.update((ROOT / rel).read_bytes())
+        for line in (ROOT / rel).read_text().splitlines():
+            code = line.split("//", 1)[0].rstrip()
+            if code:
+                h.update(code.encode() + b"\n")
     return h.hexdigest()[:16]
 
 
