@@ -100,6 +100,7 @@ size_t grouped_bytes(int ndim, int n_rec, int Dv, int interp)
     const long long nt = interp == TP_CUBIC ? 4 : 2;
     const long long per = (long long)Dv * Dv * (Dv / 2 + 1) * nt;
     if (per >= (1LL << 31)) return 0;
+    if ((long long)n_rec > (LLONG_MAX / 8) / per) return 0;  // beyond any device memory
     return (size_t)(per * n_rec * 8);
 }
 

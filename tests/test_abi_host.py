@@ -145,6 +145,10 @@ def test_workspace_size():
     assert tp.tp_workspace_size(3, 1, 7, tp.make_opts(1)) == 0        # odd box
     assert tp.tp_workspace_size(3, 1, 1024, tp.make_opts(1)) == 0     # 32-bit offsets
     assert tp.tp_workspace_size(3, 1, 128, tp.make_opts(5)) == 0      # bad interp
+    per = 1022 * 1022 * 512 * 4 * 8                                   # bytes of one volume's copy
+    assert tp.tp_workspace_size(3, 2**29, 1022, tp.make_opts(1)) == per * 2**29
+    assert tp.tp_workspace_size(3, 2**31 - 1, 1022, tp.make_opts(1)) == 0   # would overflow
+    assert tp.tp_workspace_size(3, -1, 128, tp.make_opts(1)) == 0
 
 
 def test_workspace_argument_errors():
