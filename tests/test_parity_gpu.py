@@ -149,6 +149,20 @@ def test_workspace_path(case):
     assert torch.equal(y0, y2)
 
 
+def test_workspace_ignored_in_2d():
+    """ndim = 2 has no grouped copy: a workspace passed to the backward is ignored."""
+    case = CASES[6]
+    rec, rot, shift, grad, _, kw, op = make_case(case, seed=8)
+    V, R, S, G = dev(rec), dev(rot), dev(shift), dev(grad)
+    assert tp.tp_workspace_size(2, rec.shape[0], rec.shape[1], op) == 0
+    ws = torch.empty(1 << 12, dtype=torch.uint8, device="cuda")
+    g0 = tp.project_backward(V, R, G, S, opts=op)
+    g1 = (torch.empty_like(V), torch.empty_like(R), torch.empty_like(g0[2]))
+    tp.tp_project_backward_ws(2, V, R, S, G, g1[0], g1[1], g1[2], ws, op)
+    for a, b in zip(g0, g1):
+        assert max_rel(host(b), host(a)) <= TOL_BWD
+
+
 def _bp_grads(case, with_weights, seed):
     ndim = case[0]
     Gv, rot, shift, proj, w, kw, op = make_case(case, seed=seed)
