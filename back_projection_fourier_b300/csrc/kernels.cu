@@ -110,13 +110,35 @@ __device__ void build_rowstart(const Geom& g, int* rowstart, int* scratch)
     __syncthreads();
 }
 
-// Slow-path queue: pixels packed as (row << 16) | kx.
-struct Queue {
-    int* slots;  // [2 * threads of the CTA]
+// Slow-path queue of one warp: 64 shared-memory slots of (row << 16) | kx.  The warp appends
+// its slow pixels (one ballot) and evaluates them 32 at a time, one per lane, so they do not
+// make the warp diverge; the rest are drained at the end of the work unit.  Warp-synchronous:
+// the pixel loops need no CTA-wide barrier.
+constexpr int kWarpQueue = 64;
+
+struct WarpQueue {
+    int* slots;  // this warp's kWarpQueue slots
+    int count;   // entries waiting (the same in every lane)
+
+    __device__ __forceinline__ void push(bool slow, int row, int kx)
+    {
+        const unsigned mask = __ballot_sync(0xffffffffu, slow);
+        const int lane = threadIdx.x & 31;
+        if (slow) slots[count + __popc(mask & ((1u << lane) - 1))] = (row << 16) | kx;
+        count += __popc(mask);
+        __syncwarp();
+    }
+};
+
+// Slow-path queue of a whole CTA (kept for the 3D forward, whose warps gain from staying
+// on neighbouring image rows): the CTA appends its slow pixels and, at CTA barriers,
+// evaluates them one round of threads at a time.
+struct CtaQueue {
+    int* slots;  // [kWarpQueue * warps of the CTA] = [2 * threads]
     int* count;  // shared counter
 };
 
-__device__ __forceinline__ void enqueue(Queue q, bool slow, int row, int kx)
+__device__ __forceinline__ void cta_enqueue(CtaQueue q, bool slow, int row, int kx)
 {
     const unsigned mask = __ballot_sync(0xffffffffu, slow);
     if (!mask) return;
@@ -207,13 +229,15 @@ __global__ void __launch_bounds__(kThreads, NDIM == 3 ? 3 : 4) project_kernel(
 {
     extern __shared__ int smem[];
     int* rowstart = smem;                    // [Do + 1]
-    int* qslots = smem + g.Do + 1;           // [2 * kThreads]
+    int* qslots = smem + g.Do + 1;           // [kWarpQueue per warp]
     __shared__ int scratch[kThreads / 32];
     __shared__ int qcount;
     build_rowstart(g, rowstart, scratch);
     if (threadIdx.x == 0) qcount = 0;
     __syncthreads();
-    const Queue q{qslots, &qcount};
+    const int lane = threadIdx.x & 31;
+    WarpQueue q{qslots + (threadIdx.x >> 5) * kWarpQueue, 0};  // 2D
+    const CtaQueue cq{qslots, &qcount};                         // 3D
     const int nkept = rowstart[g.Do];
     const int npix = (int)g.img_elems;
     const int chunk = kept_chunk(nkept, splits);
@@ -255,31 +279,61 @@ __global__ void __launch_bounds__(kThreads, NDIM == 3 ? 3 : 4) project_kernel(
                 else
                     slow = true;
             }
-            enqueue(q, slow, row, kx);
-            __syncthreads();
-            if (qcount >= kThreads) {
-                const int e = q.slots[qcount - kThreads + threadIdx.x];
+            if constexpr (NDIM == 3) {
+                // 3D: the CTA's warps stay on neighbouring image rows, which share L1 lines of
+                // the volume; slow pixels wait in one CTA queue, drained a round at a time
+                cta_enqueue(cq, slow, row, kx);
+                __syncthreads();
+                if (qcount >= kThreads) {
+                    const int e = cq.slots[qcount - kThreads + threadIdx.x];
+                    const int qrow = e >> 16, qkx = e & 0xffff;
+                    float2 v;
+                    eval_general<NDIM, INTERP, false>(g, V, ip.R, qkx,
+                                                      row_freq(qrow, g.Do, g.halfo, g.centered), v, nullptr);
+                    finish(qrow, qkx, v);
+                    __syncthreads();
+                    if (threadIdx.x == 0) qcount -= kThreads;
+                    __syncthreads();
+                }
+            } else {
+                // 2D: each warp runs free with its own queue
+                q.push(slow, row, kx);
+                if (q.count >= 32) {
+                    const int e = q.slots[q.count - 32 + lane];
+                    const int qrow = e >> 16, qkx = e & 0xffff;
+                    float2 v;
+                    eval_general<NDIM, INTERP, false>(g, V, ip.R, qkx,
+                                                      row_freq(qrow, g.Do, g.halfo, g.centered), v, nullptr);
+                    finish(qrow, qkx, v);
+                    q.count -= 32;
+                    __syncwarp();
+                }
+            }
+        }
+        if constexpr (NDIM == 3) {
+            if (threadIdx.x < qcount) {
+                const int e = cq.slots[threadIdx.x];
                 const int qrow = e >> 16, qkx = e & 0xffff;
                 float2 v;
                 eval_general<NDIM, INTERP, false>(g, V, ip.R, qkx,
                                                   row_freq(qrow, g.Do, g.halfo, g.centered), v, nullptr);
                 finish(qrow, qkx, v);
-                __syncthreads();
-                if (threadIdx.x == 0) qcount -= kThreads;
-                __syncthreads();
             }
+            __syncthreads();
+            if (threadIdx.x == 0) qcount = 0;
+            __syncthreads();
+        } else {
+            if (lane < q.count) {
+                const int e = q.slots[lane];
+                const int qrow = e >> 16, qkx = e & 0xffff;
+                float2 v;
+                eval_general<NDIM, INTERP, false>(g, V, ip.R, qkx,
+                                                  row_freq(qrow, g.Do, g.halfo, g.centered), v, nullptr);
+                finish(qrow, qkx, v);
+            }
+            q.count = 0;
+            __syncwarp();
         }
-        if (threadIdx.x < qcount) {
-            const int e = q.slots[threadIdx.x];
-            const int qrow = e >> 16, qkx = e & 0xffff;
-            float2 v;
-            eval_general<NDIM, INTERP, false>(g, V, ip.R, qkx,
-                                              row_freq(qrow, g.Do, g.halfo, g.centered), v, nullptr);
-            finish(qrow, qkx, v);
-        }
-        __syncthreads();
-        if (threadIdx.x == 0) qcount = 0;
-        __syncthreads();
     }
 }
 
@@ -342,14 +396,12 @@ __global__ void __launch_bounds__(kPoseThreads, 4) grad_pose_kernel(
     constexpr int NG = NDIM * 2 + 2;
     extern __shared__ int smem[];
     int* rowstart = smem;
-    int* qslots = smem + g.Do + 1;
+    int* qslots = smem + g.Do + 1;           // [kWarpQueue per warp]
     __shared__ int scratch[kPoseThreads / 32];
     __shared__ float red[kPoseThreads / 32];
-    __shared__ int qcount;
     build_rowstart<kPoseThreads>(g, rowstart, scratch);
-    if (threadIdx.x == 0) qcount = 0;
-    __syncthreads();
-    const Queue q{qslots, &qcount};
+    const int lane = threadIdx.x & 31;
+    WarpQueue q{qslots + (threadIdx.x >> 5) * kWarpQueue, 0};
     const int nkept = rowstart[g.Do];
     const int chunk = kept_chunk<kPoseThreads>(nkept, splits);
 
@@ -387,30 +439,28 @@ __global__ void __launch_bounds__(kPoseThreads, 4) grad_pose_kernel(
                 else
                     slow = true;
             }
-            enqueue(q, slow, row, kx);
-            __syncthreads();
-            if (qcount >= kPoseThreads) {
-                const int e = q.slots[qcount - kPoseThreads + threadIdx.x];
+            q.push(slow, row, kx);
+            if (q.count >= 32) {
+                const int e = q.slots[q.count - 32 + lane];
                 const int qrow = e >> 16, qkx = e & 0xffff;
                 float2 v, dv[3];
                 eval_general<NDIM, INTERP, true>(g, V, ip.R, qkx,
                                                  row_freq(qrow, g.Do, g.halfo, g.centered), v, dv);
                 add(qrow, qkx, v, dv);
-                __syncthreads();
-                if (threadIdx.x == 0) qcount -= kPoseThreads;
-                __syncthreads();
+                q.count -= 32;
+                __syncwarp();
             }
         }
-        if (threadIdx.x < qcount) {
-            const int e = q.slots[threadIdx.x];
+        if (lane < q.count) {
+            const int e = q.slots[lane];
             const int qrow = e >> 16, qkx = e & 0xffff;
             float2 v, dv[3];
             eval_general<NDIM, INTERP, true>(g, V, ip.R, qkx,
                                              row_freq(qrow, g.Do, g.halfo, g.centered), v, dv);
             add(qrow, qkx, v, dv);
         }
-        __syncthreads();
-        if (threadIdx.x == 0) qcount = 0;
+        q.count = 0;
+        __syncwarp();
         // per-item sums; several reconstructions may share one pose's parameters
         const long long ri = (long long)(g.rot_shared ? 0 : ir.r) * g.n_pose + ir.p;
         const long long si = (long long)(g.sh_shared ? 0 : ir.r) * g.n_pose + ir.p;
@@ -1248,7 +1298,7 @@ TableShape table_shape(const Geom& g, int sms, int ctas_per_sm, int threads = kT
     t.n_work = n_items * t.splits;
     const long long cap = 16LL * sms;  // persistent-style: the table is built once per CTA
     t.grid = (unsigned)(t.n_work < cap ? t.n_work : cap);
-    t.smem = (size_t)(g.Do + 1 + 2 * threads) * sizeof(int);  // kept-pixel table + slow queue
+    t.smem = (size_t)(g.Do + 1 + kWarpQueue * (threads / 32)) * sizeof(int);  // table + warp queues
     return t;
 }
 
