@@ -35,6 +35,12 @@ constexpr int kThreads = 256;
 // The pose-gradient gather runs in CTAs of 128 threads: at its 128 registers per thread that
 // is 4 CTAs per SM (4 items in flight) instead of 2, with cheaper per-item reductions.
 constexpr int kPoseThreads = 128;
+#ifndef TP_ROWS_THREADS
+#define TP_ROWS_THREADS 256
+#endif
+// The 2D owner-computes scatter: CTAs of this many threads, a thread per output row segment
+// (128 measured the same, 64 slower).
+constexpr int kRowsThreads = TP_ROWS_THREADS;
 constexpr int kMaxTableRows = 4096;  // image boxes up to this size use the kept-pixel table
 
 struct ItemRange {
@@ -576,12 +582,14 @@ struct SegMargin {
     static constexpr int AW = kSegW + 2 * ML;
 };
 
-template <int NDIM, int INTERP, bool DATA, bool WTS>
-__global__ void __launch_bounds__(kThreads) scatter_rows_kernel(
+template <int NDIM, int INTERP, bool DATA, bool WTS, int BT>
+__global__ void __launch_bounds__(BT) scatter_rows_kernel(
     const float2* __restrict__ proj, const float* __restrict__ wts,
     const float* __restrict__ rot, const float* __restrict__ shift,
     float2* __restrict__ vout, float* __restrict__ wout, Geom g, long long n_items)
 {
+    // the 3D row scan below counts at most 4 z planes per thread
+    static_assert(NDIM == 2 || 4 * BT >= kMaxScatterBox, "3D needs 4 * BT >= the largest box");
     constexpr int NT = Taps<INTERP>::N;
     constexpr int FIRST = Taps<INTERP>::first;
     constexpr float S = INTERP == kCubic ? 2.0f : 1.0f;
@@ -589,25 +597,25 @@ __global__ void __launch_bounds__(kThreads) scatter_rows_kernel(
     constexpr int ML = SegMargin<INTERP>::ML;
     constexpr int AW = SegMargin<INTERP>::AW;
     extern __shared__ __align__(16) unsigned char sm_raw[];
-    // [acc: AW x kThreads float2][wacc: AW x kThreads float][twx: Ho][twy: Do][kmax: Do]
+    // [acc: AW x BT float2][wacc: AW x BT float][twx: Ho][twy: Do][kmax: Do]
     // [rowtab: Dv+1][ylo: Dv]
     float2* acc = reinterpret_cast<float2*>(sm_raw);
-    float* wacc = reinterpret_cast<float*>(acc + (DATA ? AW * kThreads : 0));
-    float2* twx = reinterpret_cast<float2*>(wacc + (WTS ? AW * kThreads : 0));
+    float* wacc = reinterpret_cast<float*>(acc + (DATA ? AW * BT : 0));
+    float2* twx = reinterpret_cast<float2*>(wacc + (WTS ? AW * BT : 0));
     float2* twy = twx + g.Ho;
     int* kmaxt = reinterpret_cast<int*>(twy + g.Do);
     int* rowtab = kmaxt + g.Do;
     int* ylo = rowtab + g.Dv + 1;
-    __shared__ int scratch[kThreads / 32];
+    __shared__ int scratch[BT / 32];
     __shared__ float Rs[9];
     __shared__ float2 sh;
 
     for (int j = 0; j < AW; ++j) {
-        if (DATA) acc[j * kThreads + threadIdx.x] = make_float2(0.f, 0.f);
-        if (WTS) wacc[j * kThreads + threadIdx.x] = 0.f;
+        if (DATA) acc[j * BT + threadIdx.x] = make_float2(0.f, 0.f);
+        if (WTS) wacc[j * BT + threadIdx.x] = 0.f;
     }
     // last kept kx of every image row (-1: none)
-    for (int i = threadIdx.x; i < g.Do; i += kThreads) {
+    for (int i = threadIdx.x; i < g.Do; i += BT) {
         const int ky = row_freq(i, g.Do, g.halfo, g.centered);
         kmaxt[i] = row_kept(g, i) - 1;
         (void)ky;
@@ -630,11 +638,11 @@ __global__ void __launch_bounds__(kThreads) scatter_rows_kernel(
         __syncthreads();
         // separable shift twiddles: conj(phase(kx, ky)) = conj(twx[kx]) * conj(twy[row])
         if (DATA && g.has_shift) {
-            for (int k = threadIdx.x; k < g.Ho; k += kThreads) {
+            for (int k = threadIdx.x; k < g.Ho; k += BT) {
                 const float2 t = shift_phase((float)k, 0.f, sh.x, sh.y, g.Do_f, g.inv_Do);
                 twx[k] = make_float2(t.x, -t.y);
             }
-            for (int i = threadIdx.x; i < g.Do; i += kThreads) {
+            for (int i = threadIdx.x; i < g.Do; i += BT) {
                 const float2 t = shift_phase(0.f, (float)row_freq(i, g.Do, g.halfo, g.centered), sh.x,
                                              sh.y, g.Do_f, g.inv_Do);
                 twy[i] = make_float2(t.x, -t.y);
@@ -644,7 +652,7 @@ __global__ void __launch_bounds__(kThreads) scatter_rows_kernel(
         int nrows;
         if constexpr (NDIM == 3) {
             // per z plane, the y range of the slice's disk cut by the strip |c_z - u_z| < s
-            const int per = (g.Dv + kThreads - 1) / kThreads;
+            const int per = (g.Dv + BT - 1) / BT;
             const int i0 = threadIdx.x * per;
             int cnt[4] = {0, 0, 0, 0};
             int sum = 0;
@@ -673,7 +681,7 @@ __global__ void __launch_bounds__(kThreads) scatter_rows_kernel(
             __syncthreads();
             if (threadIdx.x == 0) {
                 int a = 0;
-                for (int w = 0; w < kThreads / 32; ++w) {
+                for (int w = 0; w < BT / 32; ++w) {
                     const int t = scratch[w];
                     scratch[w] = a;
                     a += t;
@@ -687,7 +695,7 @@ __global__ void __launch_bounds__(kThreads) scatter_rows_kernel(
                 rowtab[iz] = run;
                 run += cnt[k];
             }
-            if (threadIdx.x == kThreads - 1) rowtab[g.Dv] = run;
+            if (threadIdx.x == BT - 1) rowtab[g.Dv] = run;
             __syncthreads();
             nrows = rowtab[g.Dv];
         } else {
@@ -722,7 +730,7 @@ __global__ void __launch_bounds__(kThreads) scatter_rows_kernel(
         const bool sides_known = NDIM == 3 && fabsf(mdet) > 1e-3f;
         // ky ranges of the parallelogram from each pair of strips: pairs (x,y), (x,z), (y,z)
         int iz = 0;
-        for (int n = threadIdx.x; n < nrows; n += kThreads) {
+        for (int n = threadIdx.x; n < nrows; n += BT) {
             int uz = 0, uy;
             if constexpr (NDIM == 3) {
                 while (rowtab[iz + 1] <= n) ++iz;
@@ -805,12 +813,12 @@ __global__ void __launch_bounds__(kThreads) scatter_rows_kernel(
                             for (int k = 0; k < NT; ++k) {
                                 const float wk = (skip_x0 && j0 + k == ML) ? 0.f : wx[k];
                                 if constexpr (DATA) {
-                                    float2& a = acc[(j0 + k) * kThreads + threadIdx.x];
+                                    float2& a = acc[(j0 + k) * BT + threadIdx.x];
                                     a.x = fmaf(wk, s.x, a.x);
                                     a.y = fmaf(wk, s.y, a.y);
                                 }
                                 if constexpr (WTS) {
-                                    float& b = wacc[(j0 + k) * kThreads + threadIdx.x];
+                                    float& b = wacc[(j0 + k) * BT + threadIdx.x];
                                     b = fmaf(wk, sw, b);
                                 }
                             }
@@ -819,18 +827,18 @@ __global__ void __launch_bounds__(kThreads) scatter_rows_kernel(
                 }
                 // add the finished segment to the volume and clear the accumulator
                 for (int j = 0; j < ML; ++j) {
-                    if (DATA) acc[j * kThreads + threadIdx.x] = make_float2(0.f, 0.f);
-                    if (WTS) wacc[j * kThreads + threadIdx.x] = 0.f;
-                    if (DATA) acc[(ML + W + j) * kThreads + threadIdx.x] = make_float2(0.f, 0.f);
-                    if (WTS) wacc[(ML + W + j) * kThreads + threadIdx.x] = 0.f;
+                    if (DATA) acc[j * BT + threadIdx.x] = make_float2(0.f, 0.f);
+                    if (WTS) wacc[j * BT + threadIdx.x] = 0.f;
+                    if (DATA) acc[(ML + W + j) * BT + threadIdx.x] = make_float2(0.f, 0.f);
+                    if (WTS) wacc[(ML + W + j) * BT + threadIdx.x] = 0.f;
                 }
                 const int nown = min(W, g.halfv - X0 + 1);
                 if constexpr (DATA) {
                     for (int j = 0; j < nown;) {
                         float2* dst = G + roff + X0 + j;
-                        float2& a = acc[(ML + j) * kThreads + threadIdx.x];
+                        float2& a = acc[(ML + j) * BT + threadIdx.x];
                         if (j + 1 < nown && (reinterpret_cast<uintptr_t>(dst) & 15) == 0) {
-                            float2& b = acc[(ML + j + 1) * kThreads + threadIdx.x];
+                            float2& b = acc[(ML + j + 1) * BT + threadIdx.x];
                             if (a.x != 0.f || a.y != 0.f || b.x != 0.f || b.y != 0.f)
                                 atomicAdd(reinterpret_cast<float4*>(dst), make_float4(a.x, a.y, b.x, b.y));
                             a = make_float2(0.f, 0.f);
@@ -842,11 +850,11 @@ __global__ void __launch_bounds__(kThreads) scatter_rows_kernel(
                             j += 1;
                         }
                     }
-                    for (int j = nown; j < W; ++j) acc[(ML + j) * kThreads + threadIdx.x] = make_float2(0.f, 0.f);
+                    for (int j = nown; j < W; ++j) acc[(ML + j) * BT + threadIdx.x] = make_float2(0.f, 0.f);
                 }
                 if constexpr (WTS) {
                     for (int j = 0; j < W; ++j) {
-                        float& b = wacc[(ML + j) * kThreads + threadIdx.x];
+                        float& b = wacc[(ML + j) * BT + threadIdx.x];
                         if (j < nown && b != 0.f) atomicAdd(Wt + roff + X0 + j, b);
                         b = 0.f;
                     }
@@ -1374,14 +1382,14 @@ void launch_scatter_rows(const Geom& g, const float2* P, const float* weights, c
                          const float* shift, float2* VO, float* WO, int sms, cudaStream_t stream)
 {
     constexpr int AW = SegMargin<INTERP>::AW;
-    const size_t smem = (DATA ? (size_t)AW * kThreads * 8 : 0) + (WTS ? (size_t)AW * kThreads * 4 : 0) +
+    const size_t smem = (DATA ? (size_t)AW * kRowsThreads * 8 : 0) + (WTS ? (size_t)AW * kRowsThreads * 4 : 0) +
                         (size_t)(g.Ho + g.Do) * 8 + (size_t)(g.Do + 2 * g.Dv + 1) * 4;
-    auto kern = scatter_rows_kernel<NDIM, INTERP, DATA, WTS>;
+    auto kern = scatter_rows_kernel<NDIM, INTERP, DATA, WTS, kRowsThreads>;
     cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     const long long n_items = (long long)g.n_rec * g.n_pose;
-    const long long cap = 8LL * sms;
+    const long long cap = 8LL * sms * kThreads / kRowsThreads;
     const unsigned grid = (unsigned)(n_items < cap ? n_items : cap);
-    kern<<<grid, kThreads, smem, stream>>>(P, weights, rot, shift, VO, WO, g, n_items);
+    kern<<<grid, kRowsThreads, smem, stream>>>(P, weights, rot, shift, VO, WO, g, n_items);
 }
 
 template <int INTERP, bool DATA, bool WTS>
@@ -1419,14 +1427,14 @@ void launch_backproject_t(const Geom& g, const float2* P, const float* weights, 
             launch_scatter_tile<INTERP, true, false>(g, P, weights, rot, shift, VO, WO, sms, stream);
         else
             launch_scatter_tile<INTERP, false, true>(g, P, weights, rot, shift, VO, WO, sms, stream);
-        return;
+    } else {
+        if (VO && WO)
+            launch_scatter_rows<NDIM, INTERP, true, true>(g, P, weights, rot, shift, VO, WO, sms, stream);
+        else if (VO)
+            launch_scatter_rows<NDIM, INTERP, true, false>(g, P, weights, rot, shift, VO, WO, sms, stream);
+        else
+            launch_scatter_rows<NDIM, INTERP, false, true>(g, P, weights, rot, shift, VO, WO, sms, stream);
     }
-    if (VO && WO)
-        launch_scatter_rows<NDIM, INTERP, true, true>(g, P, weights, rot, shift, VO, WO, sms, stream);
-    else if (VO)
-        launch_scatter_rows<NDIM, INTERP, true, false>(g, P, weights, rot, shift, VO, WO, sms, stream);
-    else
-        launch_scatter_rows<NDIM, INTERP, false, true>(g, P, weights, rot, shift, VO, WO, sms, stream);
 }
 
 template <int NDIM, int INTERP>
