@@ -35,6 +35,9 @@ constexpr int kThreads = 256;
 // The pose-gradient gather runs in CTAs of 128 threads: at its 128 registers per thread that
 // is 4 CTAs per SM (4 items in flight) instead of 2, with cheaper per-item reductions.
 constexpr int kPoseThreads = 128;
+// The 3D forward gather: CTAs of 192 threads, 4 per SM (24 warps): cheaper CTA barriers
+// around its shared slow-pixel queue than 256 x 3, with the same registers per thread.
+constexpr int kFwd3Threads = 192;
 #ifndef TP_ROWS_THREADS
 #define TP_ROWS_THREADS 256
 #endif
@@ -228,17 +231,18 @@ __device__ __forceinline__ bool eval_fast(const Geom& g, const float2* __restric
 // ------------------------------------------------------------------ forward ----
 
 template <int NDIM, int INTERP, int WIN>
-__global__ void __launch_bounds__(kThreads, NDIM == 3 ? 3 : 4) project_kernel(
+__global__ void __launch_bounds__(NDIM == 3 ? kFwd3Threads : kThreads, 4) project_kernel(
     const float2* __restrict__ rec, const float* __restrict__ rot,
     const float* __restrict__ shift, float2* __restrict__ out, Geom g, int splits, long long n_work,
     const float2* __restrict__ grouped)
 {
+    constexpr int BT = NDIM == 3 ? kFwd3Threads : kThreads;  // threads of the CTA
     extern __shared__ int smem[];
     int* rowstart = smem;                    // [Do + 1]
     int* qslots = smem + g.Do + 1;           // [kWarpQueue per warp]
-    __shared__ int scratch[kThreads / 32];
+    __shared__ int scratch[BT / 32];
     __shared__ int qcount;
-    build_rowstart(g, rowstart, scratch);
+    build_rowstart<BT>(g, rowstart, scratch);
     if (threadIdx.x == 0) qcount = 0;
     __syncthreads();
     const int lane = threadIdx.x & 31;
@@ -246,7 +250,7 @@ __global__ void __launch_bounds__(kThreads, NDIM == 3 ? 3 : 4) project_kernel(
     const CtaQueue cq{qslots, &qcount};                         // 3D
     const int nkept = rowstart[g.Do];
     const int npix = (int)g.img_elems;
-    const int chunk = kept_chunk(nkept, splits);
+    const int chunk = kept_chunk<BT>(nkept, splits);
 
     // work unit = (item, part): part takes one chunk of the item's kept pixels
     for (long long w = blockIdx.x; w < n_work; w += gridDim.x) {
@@ -257,7 +261,7 @@ __global__ void __launch_bounds__(kThreads, NDIM == 3 ? 3 : 4) project_kernel(
         const float2* VG = WIN == kGrouped ? grouped + (long long)Taps<INTERP>::N * ir.r * g.rec_elems : V;
         float2* y = out + ir.item * g.img_elems;
         // pixels beyond the cutoff are zero
-        for (int p = ir.part * kThreads + threadIdx.x; p < npix; p += splits * kThreads) {
+        for (int p = ir.part * BT + threadIdx.x; p < npix; p += splits * BT) {
             int i, j;
             split_pixel(p, g.Ho, i, j);
             if (j >= rowstart[i + 1] - rowstart[i]) y[p] = make_float2(0.f, 0.f);
@@ -270,7 +274,7 @@ __global__ void __launch_bounds__(kThreads, NDIM == 3 ? 3 : 4) project_kernel(
         };
         const int b0 = ir.part * chunk, b1 = min(nkept, b0 + chunk);
         int row = b0 < nkept ? row_of_kept(rowstart, g.Do, b0) : 0;
-        for (int base = b0; base < b1; base += kThreads) {
+        for (int base = b0; base < b1; base += BT) {
             const int n = base + threadIdx.x;
             bool slow = false;
             int kx = 0;
@@ -290,15 +294,15 @@ __global__ void __launch_bounds__(kThreads, NDIM == 3 ? 3 : 4) project_kernel(
                 // the volume; slow pixels wait in one CTA queue, drained a round at a time
                 cta_enqueue(cq, slow, row, kx);
                 __syncthreads();
-                if (qcount >= kThreads) {
-                    const int e = cq.slots[qcount - kThreads + threadIdx.x];
+                if (qcount >= BT) {
+                    const int e = cq.slots[qcount - BT + threadIdx.x];
                     const int qrow = e >> 16, qkx = e & 0xffff;
                     float2 v;
                     eval_general<NDIM, INTERP, false>(g, V, ip.R, qkx,
                                                       row_freq(qrow, g.Do, g.halfo, g.centered), v, nullptr);
                     finish(qrow, qkx, v);
                     __syncthreads();
-                    if (threadIdx.x == 0) qcount -= kThreads;
+                    if (threadIdx.x == 0) qcount -= BT;
                     __syncthreads();
                 }
             } else {
@@ -1320,9 +1324,9 @@ template <int NDIM, int INTERP, int WIN>
 void launch_project_table(const Geom& g, const float2* R, const float* rot, const float* shift,
                           float2* Y, const float2* grouped, int sms, cudaStream_t stream)
 {
-    // 3 resident CTAs per SM leave each 3D projection more L1; 2D images prefer 4
-    const TableShape t = table_shape(g, sms, NDIM == 3 ? 3 : 4);
-    project_kernel<NDIM, INTERP, WIN><<<t.grid, kThreads, t.smem, stream>>>(
+    constexpr int BT = NDIM == 3 ? kFwd3Threads : kThreads;
+    const TableShape t = table_shape(g, sms, 4, BT);
+    project_kernel<NDIM, INTERP, WIN><<<t.grid, BT, t.smem, stream>>>(
         R, rot, shift, Y, g, t.splits, t.n_work, grouped);
 }
 
