@@ -254,6 +254,37 @@ def kept_pixels(wl) -> int:
     return int(((kx[None, :] ** 2 + ky[:, None] ** 2) <= wl.rc ** 2).sum())
 
 
+def host_link(b, hG, s_in, s_out, h2d, d2h, step_s) -> dict:
+    """Host-link rates on the end-to-end step's own pinned buffers, best of three: the
+    upstream gradient in alone, the projections out alone, and both at once.  A step that
+    moves h2d bytes in and d2h bytes out takes at least the two-way time scaled to them."""
+    import torch
+
+    n_in = hG.numel() * hG.element_size()
+    n_out = b["Y"].numel() * b["Y"].element_size()
+
+    def timed(copy_in, copy_out):
+        best = float("inf")
+        for _ in range(3):
+            torch.cuda.synchronize()
+            t0 = time.perf_counter()
+            if copy_in:
+                with torch.cuda.stream(s_in):
+                    b["dG"].copy_(hG, non_blocking=True)
+            if copy_out:
+                with torch.cuda.stream(s_out):
+                    b["oY"].copy_(b["Y"], non_blocking=True)
+            torch.cuda.synchronize()
+            best = min(best, time.perf_counter() - t0)
+        return best
+
+    t_in, t_out, t_both = timed(True, False), timed(False, True), timed(True, True)
+    floor_s = t_both * max(h2d / n_in, d2h / n_out)
+    return {"h2d_GBps": n_in / t_in / 1e9, "d2h_GBps": n_out / t_out / 1e9,
+            "both_ways_GBps": [n_in / t_both / 1e9, n_out / t_both / 1e9],
+            "floor_ms_per_step": 1e3 * floor_s, "frac": floor_s / step_s}
+
+
 def run_ours(args, wl):
     import torch
     import torch.distributed as dist
@@ -352,12 +383,22 @@ def run_ours(args, wl):
     if not args.no_e2e:
         hV, hR, hG = V.cpu().pin_memory(), R.cpu().pin_memory(), G.cpu().pin_memory()
         hS = S.cpu().pin_memory() if S is not None else None
-        oY = torch.empty(Y.shape, dtype=Y.dtype, pin_memory=True)
-        ogV = torch.empty(gV.shape, dtype=gV.dtype, pin_memory=True)
-        ogR = torch.empty(gR.shape, dtype=gR.dtype, pin_memory=True)
-        ogS = torch.empty(gS.shape, dtype=gS.dtype, pin_memory=True)
-        dV, dR, dG = torch.empty_like(V), torch.empty_like(R), torch.empty_like(G)
-        dS = torch.empty_like(S) if S is not None else None
+
+        # Two buffer sets, device and host side, used by alternate steps, so that one step's
+        # host->device copies and the previous step's device->host copies overlap the kernels
+        # of their neighbours instead of waiting for them.
+        def buffer_set(first):
+            b = {"Y": Y, "gV": gV, "gR": gR, "gS": gS, "WS": WS} if first else {
+                "Y": torch.empty_like(Y), "gV": torch.empty_like(gV), "gR": torch.empty_like(gR),
+                "gS": torch.empty_like(gS), "WS": None if WS is None else torch.empty_like(WS)}
+            b.update(dV=torch.empty_like(V), dR=torch.empty_like(R), dG=torch.empty_like(G),
+                     dS=torch.empty_like(S) if S is not None else None)
+            b.update(oY=torch.empty(Y.shape, dtype=Y.dtype, pin_memory=True),
+                     ogV=torch.empty(gV.shape, dtype=gV.dtype, pin_memory=True),
+                     ogR=torch.empty(gR.shape, dtype=gR.dtype, pin_memory=True),
+                     ogS=torch.empty(gS.shape, dtype=gS.dtype, pin_memory=True))
+            return b
+        bufs = [buffer_set(True), buffer_set(False)]
 
         # Pipelined over chunks of poses on three streams: the host->device copy of chunk c+1
         # and the device->host copy of chunk c-1 overlap the kernels of chunk c.  Per chunk:
@@ -371,41 +412,51 @@ def run_ours(args, wl):
         ev_in = [torch.cuda.Event() for _ in bounds]
         ev_done = [torch.cuda.Event() for _ in bounds]
         ev_vol = torch.cuda.Event()
+        # per buffer set: its inputs were last read (kernels done) / its outputs last copied out
+        ev_read = [torch.cuda.Event() for _ in bufs]
+        ev_out = [torch.cuda.Event() for _ in bufs]
         sl = lambda t, a, b: None if t is None else t[:, a:b]  # noqa: E731
+        n_e2e = [0]
 
         def e2e_step():
+            k = n_e2e[0] % 2
+            n_e2e[0] += 1
+            b = bufs[k]
+            dV, dR, dG, dS = b["dV"], b["dR"], b["dG"], b["dS"]
             with torch.cuda.stream(s_in):
+                s_in.wait_event(ev_read[k])
                 dV.copy_(hV, non_blocking=True)
                 dR.copy_(hR, non_blocking=True)
                 if dS is not None:
                     dS.copy_(hS, non_blocking=True)
                 ev_v.record(s_in)
-                for c, (a, b) in enumerate(bounds):
-                    dG[:, a:b].copy_(hG[:, a:b], non_blocking=True)
+                for c, (a, bb) in enumerate(bounds):
+                    dG[:, a:bb].copy_(hG[:, a:bb], non_blocking=True)
                     ev_in[c].record(s_in)
             stream.wait_event(ev_v)
-            for c, (a, b) in enumerate(bounds):
+            stream.wait_event(ev_out[k])
+            for c, (a, bb) in enumerate(bounds):
                 stream.wait_event(ev_in[c])
-                Rc, Sc, Gc = sl(dR, a, b), sl(dS, a, b), sl(dG, a, b)
-                tp.tp_project_3d_to_2d_ws(dV, Rc, Sc, Y[:, a:b], WS, op, stream)
-                tp.tp_project_backward_ws(3, dV, Rc, Sc, Gc, None, gR[:, a:b], gS[:, a:b], WS, op,
-                                          stream)
-                tp.tp_backproject_2d_to_3d(Gc, None, Rc, Sc, gV, None, wl.D, c > 0, op, stream)
+                Rc, Sc, Gc = sl(dR, a, bb), sl(dS, a, bb), sl(dG, a, bb)
+                tp.tp_project_3d_to_2d_ws(dV, Rc, Sc, b["Y"][:, a:bb], b["WS"], op, stream)
+                tp.tp_project_backward_ws(3, dV, Rc, Sc, Gc, None, b["gR"][:, a:bb],
+                                          b["gS"][:, a:bb], b["WS"], op, stream)
+                tp.tp_backproject_2d_to_3d(Gc, None, Rc, Sc, b["gV"], None, wl.D, c > 0, op,
+                                           stream)
                 ev_done[c].record(stream)
+            ev_read[k].record(stream)
             if world > 1:
-                dist.all_reduce(torch.view_as_real(gV))
+                dist.all_reduce(torch.view_as_real(b["gV"]))
             ev_vol.record(stream)
             with torch.cuda.stream(s_out):
-                for c, (a, b) in enumerate(bounds):
+                for c, (a, bb) in enumerate(bounds):
                     s_out.wait_event(ev_done[c])
-                    oY[:, a:b].copy_(Y[:, a:b], non_blocking=True)
-                    ogR[:, a:b].copy_(gR[:, a:b], non_blocking=True)
-                    ogS[:, a:b].copy_(gS[:, a:b], non_blocking=True)
+                    b["oY"][:, a:bb].copy_(b["Y"][:, a:bb], non_blocking=True)
+                    b["ogR"][:, a:bb].copy_(b["gR"][:, a:bb], non_blocking=True)
+                    b["ogS"][:, a:bb].copy_(b["gS"][:, a:bb], non_blocking=True)
                 s_out.wait_event(ev_vol)
-                ogV.copy_(gV, non_blocking=True)
-            # the next step's copies into the device inputs wait for this step's kernels
-            s_in.wait_stream(stream)
-            stream.wait_stream(s_out)
+                b["ogV"].copy_(b["gV"], non_blocking=True)
+                ev_out[k].record(s_out)
 
         for _ in range(max(1, args.warmup)):
             e2e_step()
@@ -421,10 +472,20 @@ def run_ours(args, wl):
             t = torch.tensor([dt], device=dev)
             dist.all_reduce(t, op=dist.ReduceOp.MAX)
             dt = float(t.item())
+        # both buffer sets ran the same inputs: their host results must agree (the forward
+        # exactly, the gradients up to the order of their float sums)
+        if n_e2e[0] >= 2:
+            h0, h1 = bufs[0], bufs[1]
+            rel = lambda n: float((h0[n] - h1[n]).abs().max()  # noqa: E731
+                                  / h0[n].abs().max().clamp_min(1e-30))
+            errs = {n: rel(n) for n in ("ogV", "ogR", "ogS")}
+            if not torch.equal(h0["oY"], h1["oY"]) or max(errs.values()) > 1e-5:
+                raise RuntimeError(f"e2e buffer sets disagree: {errs}")
         h2d = sum(x.numel() * x.element_size() for x in (hV, hR, hG) + ((hS,) if hS is not None else ()))
-        d2h = sum(x.numel() * x.element_size() for x in (oY, ogV, ogR, ogS))
+        d2h = sum(bufs[0][n].numel() * bufs[0][n].element_size() for n in ("oY", "ogV", "ogR", "ogS"))
         e2e = {"value": wl.B * world / (dt / args.steps), "unit": "projections/s",
                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h}
+        e2e["host_link"] = host_link(bufs[0], hG, s_in, s_out, h2d, d2h, dt / args.steps)
 
     # roofline of the dominant kernel
     dom = max(kms, key=kms.get)
