@@ -528,11 +528,16 @@ def run_ours(args, wl):
         rate, sample = oracle_rate(wl, args.cpu_sample, cores())
         cpu = {"value": rate, "unit": "projections/s", "cores": cores(), "kind": "oracle",
                "sample": sample}
+        # the same oracle on one host thread, on a sixteenth of the sample
+        rate1, sample1 = oracle_rate(wl, max(64, args.cpu_sample // 16), 1)
+        cpu["one_core"] = {"value": rate1, "unit": "projections/s", "cores": 1,
+                           "sample": sample1}
 
     if rank == 0:
         line = {
             "metric": metric_for(wl), "value": value, "unit": "projections/s", "n_gpus": world,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_step,
+            "ms_per_step_median": statistics.median(e[0].elapsed_time(e[3]) for e in evs),
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
             "data": "synthetic (seeded rfft of N(0,1) volume, uniform SO(3), CN(0,1) upstream grad)",
             "config": workload_config(wl, l2_note),

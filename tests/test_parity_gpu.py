@@ -167,6 +167,51 @@ def test_workspace_ignored_in_2d():
         assert max_rel(host(b), host(a)) <= TOL_BWD
 
 
+# rotations per reconstruction with one shared set of shifts, and the reverse
+MIXED = [(ndim, n_rot, n_sh) for ndim in (3, 2) for n_rot, n_sh in ((3, 1), (1, 3))]
+
+
+@pytest.mark.parametrize("ndim,n_rot,n_sh", MIXED)
+def test_mixed_pose_broadcast(ndim, n_rot, n_sh):
+    """Rotations and shifts broadcast over the reconstructions independently (n_rot and n_sh
+    each 1 or n_rec): every entry point, the gradient of the shared array summed over the
+    reconstructions, on the plain and the workspace calls."""
+    rng = np.random.default_rng(40 + 10 * ndim + n_rot)
+    n_rec, n_pose, D = 3, 9, 26
+    H = D // 2 + 1
+    rec = crandn32(rng, (n_rec, D, D, H) if ndim == 3 else (n_rec, D, H))
+    rot = rotations(rng, n_rot * n_pose, ndim).reshape(n_rot, n_pose, ndim, ndim)
+    shift = rng.uniform(-6, 6, (n_sh, n_pose, 2)).astype(np.float32)
+    grad = crandn32(rng, (n_rec, n_pose, D, H))
+    w = rng.uniform(0.0, 2.0, (n_rec, n_pose, D, H)).astype(np.float32)
+    kw = dict(interp=1, layout=1, oversampling=1.0, cutoff=-1.0)
+    op = opts(1, 1, 1.0, -1.0)
+    V, R, S, G = dev(rec), dev(rot), dev(shift), dev(grad)
+
+    y = tp.project(V, R, S, Do=D, opts=op)
+    assert max_rel(host(y), oracle.project(ndim, rec, rot, shift, Do=D, **kw)) <= TOL_FWD
+    r_rec, r_rot, r_sh = oracle.project_backward(ndim, rec, rot, grad, shift, **kw)
+    g_rec, g_rot, g_sh = tp.project_backward(V, R, G, S, want_shift=True, opts=op)
+    assert g_rot.shape == R.shape and g_sh.shape == S.shape
+    assert max_rel(host(g_rec), r_rec) <= TOL_BWD
+    assert max_rel(host(g_rot), r_rot) <= TOL_BWD
+    assert max_rel(host(g_sh), r_sh) <= TOL_BWD
+    vol, wvol = tp.backproject(G, R, S, dev(w), Dv=D, opts=op, ndim=ndim)
+    r_vol, r_w = oracle.backproject(ndim, grad, rot, weights=w, shift=shift, Dv=D, **kw)
+    assert max_rel(host(vol), r_vol) <= TOL_BWD
+    assert max_rel(host(wvol), r_w) <= TOL_BWD
+    if ndim == 3:
+        ws = tp.workspace_for(V, op)
+        y1 = torch.empty_like(y)
+        tp.tp_project_3d_to_2d_ws(V, R, S, y1, ws, op)
+        assert torch.equal(y, y1)
+        g1 = (torch.empty_like(V), torch.empty_like(R), torch.empty_like(S))
+        tp.tp_project_backward_ws(3, V, R, S, G, g1[0], g1[1], g1[2], ws, op)
+        assert max_rel(host(g1[0]), r_rec) <= TOL_BWD
+        assert max_rel(host(g1[1]), r_rot) <= TOL_BWD
+        assert max_rel(host(g1[2]), r_sh) <= TOL_BWD
+
+
 def _bp_grads(case, with_weights, seed):
     ndim = case[0]
     Gv, rot, shift, proj, w, kw, op = make_case(case, seed=seed)
