@@ -179,7 +179,7 @@ tp_status tp_project_backward_ws(int ndim, const void* rec, int n_rec, int Dv, c
  *   exits.  Sizes whose grouped copy needs more (tp_workspace_size above 34078720) return
  *   TP_ERR_SHAPE before anything is enqueued.  The call allocates nothing.
  *   The first call on a device looks up the array's device address (cudaGetSymbolAddress)
- *   and keeps it; make that first call before any stream capture begins.
+ *   and keeps it for the later calls.
  *   All calls share the one array and each overwrites what it reads, so calls whose work
  *   overlaps on the GPU (other streams, other host threads) race and must be ordered by
  *   the caller. */
