@@ -100,7 +100,7 @@ def _stream(stream):
     return ctypes.c_void_p(stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream))
 
 
-def _need(t, dtype, name, ndim=None):
+def _need(t, dtype, name):
     if t is None:
         return
     if t.dtype != dtype:
@@ -109,17 +109,45 @@ def _need(t, dtype, name, ndim=None):
         raise TypeError(f"{name} must be a CUDA tensor")
     if not t.is_contiguous():
         raise ValueError(f"{name} must be contiguous")
-    if ndim is not None and t.dim() != ndim:
-        raise ValueError(f"{name} must have {ndim} dimensions, got {tuple(t.shape)}")
+
+
+def _sz(t, i):
+    """Size of axis i of t, or -1 (no such axis, or no tensor): a size that fails every check."""
+    return t.shape[i] if t is not None and t.dim() > i else -1
+
+
+def _rec_shape(n_rec, D, ndim):
+    return (n_rec, D, D, D // 2 + 1) if ndim == 3 else (n_rec, D, D // 2 + 1)
+
+
+def _img_shape(n_rec, n_pose, Do):
+    return (n_rec, n_pose, Do, Do // 2 + 1)
+
+
+def _check(*items):
+    """items: (tensor or None, dtype, name, expected shape).  Every shape is checked before any
+    dtype or device, so a tensor whose shape disagrees with the sizes the call passes to the
+    library is refused on any device: the kernels index the buffers by those sizes."""
+    for t, _, name, shape in items:
+        if t is not None and tuple(t.shape) != tuple(shape):
+            raise ValueError(f"{name} must have shape {tuple(shape)}, got {tuple(t.shape)}")
+    for t, dtype, name, _ in items:
+        _need(t, dtype, name)
 
 
 def _rs(rot, shift, k):
-    _need(rot, torch.float32, "rot", 4)
-    if tuple(rot.shape[2:]) != (k, k):
-        raise ValueError(f"rot must be [n_rot][n_pose][{k}][{k}]")
-    _need(shift, torch.float32, "shift", 3)
-    n_sh = 1 if shift is None else shift.shape[0]
-    return rot.shape[0], rot.shape[1], n_sh
+    """(n_rot, n_pose, n_sh) and the check items of rot [n_rot][n_pose][k][k] and shift
+    [n_sh][n_pose][2]."""
+    n_rot, n_pose = _sz(rot, 0), _sz(rot, 1)
+    n_sh = 1 if shift is None else _sz(shift, 0)
+    items = [(rot, torch.float32, "rot", (n_rot, n_pose, k, k)),
+             (shift, torch.float32, "shift", (n_sh, n_pose, 2))]
+    return n_rot, n_pose, n_sh, items
+
+
+def _gshift(grad_shift, shift, n_sh, n_pose):
+    """Check item of a shift gradient: [n_sh][n_pose][2], or [1][n_pose][2] without shift."""
+    return (grad_shift, torch.float32, "grad_shift", (n_sh if shift is not None else 1, n_pose, 2))
 
 
 def _call(status: int, what: str):
@@ -133,32 +161,44 @@ def _opts(opts):
 
 # ------------------------------------------------------- C entry points ----
 
+def _project_checks(ndim, vol, rot, shift, out, vname):
+    n_rot, n_pose, n_sh, items = _rs(rot, shift, ndim)
+    n_rec, Dv, Do = _sz(vol, 0), _sz(vol, 1), _sz(out, 2)
+    _check((vol, torch.complex64, vname, _rec_shape(n_rec, Dv, ndim)),
+           (out, torch.complex64, "out", _img_shape(n_rec, n_pose, Do)), *items)
+    return n_rec, Dv, n_rot, n_pose, n_sh, Do
+
+
 def tp_project_3d_to_2d(vol, rot, shift, out, opts=None, stream=None):
-    _need(vol, torch.complex64, "vol", 4)
-    _need(out, torch.complex64, "out", 4)
-    n_rot, n_pose, n_sh = _rs(rot, shift, 3)
-    _call(_LIB.tp_project_3d_to_2d(_ptr(vol), vol.shape[0], vol.shape[1], _ptr(rot), n_rot, n_pose,
-                                   _ptr(shift), n_sh, _ptr(out), out.shape[2], _opts(opts),
+    n_rec, Dv, n_rot, n_pose, n_sh, Do = _project_checks(3, vol, rot, shift, out, "vol")
+    _call(_LIB.tp_project_3d_to_2d(_ptr(vol), n_rec, Dv, _ptr(rot), n_rot, n_pose,
+                                   _ptr(shift), n_sh, _ptr(out), Do, _opts(opts),
                                    _stream(stream)), "tp_project_3d_to_2d")
 
 
 def tp_project_2d_to_2d(img, rot, shift, out, opts=None, stream=None):
-    _need(img, torch.complex64, "img", 3)
-    _need(out, torch.complex64, "out", 4)
-    n_rot, n_pose, n_sh = _rs(rot, shift, 2)
-    _call(_LIB.tp_project_2d_to_2d(_ptr(img), img.shape[0], img.shape[1], _ptr(rot), n_rot, n_pose,
-                                   _ptr(shift), n_sh, _ptr(out), out.shape[2], _opts(opts),
+    n_rec, Dv, n_rot, n_pose, n_sh, Do = _project_checks(2, img, rot, shift, out, "img")
+    _call(_LIB.tp_project_2d_to_2d(_ptr(img), n_rec, Dv, _ptr(rot), n_rot, n_pose,
+                                   _ptr(shift), n_sh, _ptr(out), Do, _opts(opts),
                                    _stream(stream)), "tp_project_2d_to_2d")
+
+
+def _backproject_checks(ndim, proj, weights, rot, shift, vol_out, wvol_out, Dv, names):
+    n_rot, n_pose, n_sh, items = _rs(rot, shift, ndim)
+    ref = proj if proj is not None else weights   # proj may be absent when only weights go in
+    n_rec, Do = _sz(ref, 0), _sz(ref, 2)
+    img, rec = _img_shape(n_rec, n_pose, Do), _rec_shape(n_rec, int(Dv), ndim)
+    _check((proj, torch.complex64, "proj", img), (weights, torch.float32, "weights", img),
+           (vol_out, torch.complex64, names[0], rec), (wvol_out, torch.float32, names[1], rec),
+           *items)
+    return n_rec, Do, n_rot, n_pose, n_sh
 
 
 def tp_backproject_2d_to_3d(proj, weights, rot, shift, vol_out, wvol_out, Dv, accumulate=False,
                             opts=None, stream=None):
-    _need(proj, torch.complex64, "proj", 4)
-    _need(weights, torch.float32, "weights", 4)
-    _need(vol_out, torch.complex64, "vol_out", 4)
-    _need(wvol_out, torch.float32, "wvol_out", 4)
-    n_rot, n_pose, n_sh = _rs(rot, shift, 3)
-    _call(_LIB.tp_backproject_2d_to_3d(_ptr(proj), _ptr(weights), proj.shape[0], proj.shape[2],
+    n_rec, Do, n_rot, n_pose, n_sh = _backproject_checks(3, proj, weights, rot, shift, vol_out,
+                                                         wvol_out, Dv, ("vol_out", "wvol_out"))
+    _call(_LIB.tp_backproject_2d_to_3d(_ptr(proj), _ptr(weights), n_rec, Do,
                                        _ptr(rot), n_rot, n_pose, _ptr(shift), n_sh, _ptr(vol_out),
                                        _ptr(wvol_out), int(Dv), int(bool(accumulate)), _opts(opts),
                                        _stream(stream)), "tp_backproject_2d_to_3d")
@@ -166,49 +206,56 @@ def tp_backproject_2d_to_3d(proj, weights, rot, shift, vol_out, wvol_out, Dv, ac
 
 def tp_backproject_2d_to_2d(proj, weights, rot, shift, img_out, wimg_out, Dv, accumulate=False,
                             opts=None, stream=None):
-    _need(proj, torch.complex64, "proj", 4)
-    _need(weights, torch.float32, "weights", 4)
-    _need(img_out, torch.complex64, "img_out", 3)
-    _need(wimg_out, torch.float32, "wimg_out", 3)
-    n_rot, n_pose, n_sh = _rs(rot, shift, 2)
-    _call(_LIB.tp_backproject_2d_to_2d(_ptr(proj), _ptr(weights), proj.shape[0], proj.shape[2],
+    n_rec, Do, n_rot, n_pose, n_sh = _backproject_checks(2, proj, weights, rot, shift, img_out,
+                                                         wimg_out, Dv, ("img_out", "wimg_out"))
+    _call(_LIB.tp_backproject_2d_to_2d(_ptr(proj), _ptr(weights), n_rec, Do,
                                        _ptr(rot), n_rot, n_pose, _ptr(shift), n_sh, _ptr(img_out),
                                        _ptr(wimg_out), int(Dv), int(bool(accumulate)), _opts(opts),
                                        _stream(stream)), "tp_backproject_2d_to_2d")
 
 
+def _backward_checks(ndim, rec, rot, shift, grad_out, grad_rec, grad_rot, grad_shift):
+    n_rot, n_pose, n_sh, items = _rs(rot, shift, ndim)
+    n_rec, Dv, Do = _sz(rec, 0), _sz(rec, 1), _sz(grad_out, 2)
+    rshape = _rec_shape(n_rec, Dv, ndim)
+    _check((rec, torch.complex64, "rec", rshape),
+           (grad_out, torch.complex64, "grad_out", _img_shape(n_rec, n_pose, Do)),
+           (grad_rec, torch.complex64, "grad_rec", rshape),
+           (grad_rot, torch.float32, "grad_rot", (n_rot, n_pose, ndim, ndim)),
+           _gshift(grad_shift, shift, n_sh, n_pose), *items)
+    return n_rec, Dv, n_rot, n_pose, n_sh, Do
+
+
 def tp_project_backward(ndim, rec, rot, shift, grad_out, grad_rec, grad_rot, grad_shift,
                         opts=None, stream=None):
-    _need(rec, torch.complex64, "rec", ndim + 1)
-    _need(grad_out, torch.complex64, "grad_out", 4)
-    _need(grad_rec, torch.complex64, "grad_rec", ndim + 1)
-    _need(grad_rot, torch.float32, "grad_rot", 4)
-    _need(grad_shift, torch.float32, "grad_shift", 3)
-    n_rot, n_pose, n_sh = _rs(rot, shift, ndim)
-    _call(_LIB.tp_project_backward(int(ndim), _ptr(rec), rec.shape[0], rec.shape[1], _ptr(rot), n_rot,
-                                   n_pose, _ptr(shift), n_sh, _ptr(grad_out), grad_out.shape[2],
+    n_rec, Dv, n_rot, n_pose, n_sh, Do = _backward_checks(ndim, rec, rot, shift, grad_out,
+                                                          grad_rec, grad_rot, grad_shift)
+    _call(_LIB.tp_project_backward(int(ndim), _ptr(rec), n_rec, Dv, _ptr(rot), n_rot,
+                                   n_pose, _ptr(shift), n_sh, _ptr(grad_out), Do,
                                    _ptr(grad_rec), _ptr(grad_rot), _ptr(grad_shift), _opts(opts),
                                    _stream(stream)), "tp_project_backward")
 
 
 def tp_backproject_backward(ndim, proj, weights, rot, shift, grad_vol, grad_wvol, grad_proj,
                             grad_weights, grad_rot, grad_shift, opts=None, stream=None):
-    _need(proj, torch.complex64, "proj", 4)
-    _need(weights, torch.float32, "weights", 4)
-    _need(grad_vol, torch.complex64, "grad_vol", ndim + 1)
-    _need(grad_wvol, torch.float32, "grad_wvol", ndim + 1)
-    _need(grad_proj, torch.complex64, "grad_proj", 4)
-    _need(grad_weights, torch.float32, "grad_weights", 4)
-    _need(grad_rot, torch.float32, "grad_rot", 4)
-    _need(grad_shift, torch.float32, "grad_shift", 3)
-    n_rot, n_pose, n_sh = _rs(rot, shift, ndim)
-    ref = next(t for t in (proj, grad_proj, grad_weights, weights) if t is not None)
+    n_rot, n_pose, n_sh, items = _rs(rot, shift, ndim)
+    ref = next((t for t in (proj, grad_proj, grad_weights, weights) if t is not None), None)
     vref = grad_vol if grad_vol is not None else grad_wvol
-    if vref is None:
-        raise ValueError("grad_vol and grad_wvol are both None: the volume size is unknown")
-    _call(_LIB.tp_backproject_backward(int(ndim), _ptr(proj), _ptr(weights), ref.shape[0],
-                                       ref.shape[2], _ptr(rot), n_rot, n_pose, _ptr(shift), n_sh,
-                                       _ptr(grad_vol), _ptr(grad_wvol), vref.shape[1],
+    if ref is None or vref is None:
+        raise ValueError("the image size needs one of proj, grad_proj, grad_weights, weights and "
+                         "the volume size one of grad_vol, grad_wvol")
+    n_rec, Do, Dv = _sz(ref, 0), _sz(ref, 2), _sz(vref, 1)
+    img, vol = _img_shape(n_rec, n_pose, Do), _rec_shape(n_rec, Dv, ndim)
+    _check((proj, torch.complex64, "proj", img), (weights, torch.float32, "weights", img),
+           (grad_vol, torch.complex64, "grad_vol", vol),
+           (grad_wvol, torch.float32, "grad_wvol", vol),
+           (grad_proj, torch.complex64, "grad_proj", img),
+           (grad_weights, torch.float32, "grad_weights", img),
+           (grad_rot, torch.float32, "grad_rot", (n_rot, n_pose, ndim, ndim)),
+           _gshift(grad_shift, shift, n_sh, n_pose), *items)
+    _call(_LIB.tp_backproject_backward(int(ndim), _ptr(proj), _ptr(weights), n_rec,
+                                       Do, _ptr(rot), n_rot, n_pose, _ptr(shift), n_sh,
+                                       _ptr(grad_vol), _ptr(grad_wvol), Dv,
                                        _ptr(grad_proj), _ptr(grad_weights), _ptr(grad_rot),
                                        _ptr(grad_shift), _opts(opts), _stream(stream)),
           "tp_backproject_backward")
@@ -227,52 +274,46 @@ def _ws(workspace):
 
 
 def tp_project_3d_to_2d_ws(vol, rot, shift, out, workspace, opts=None, stream=None):
-    _need(vol, torch.complex64, "vol", 4)
-    _need(out, torch.complex64, "out", 4)
-    n_rot, n_pose, n_sh = _rs(rot, shift, 3)
+    n_rec, Dv, n_rot, n_pose, n_sh, Do = _project_checks(3, vol, rot, shift, out, "vol")
     wp, wb = _ws(workspace)
-    _call(_LIB.tp_project_3d_to_2d_ws(_ptr(vol), vol.shape[0], vol.shape[1], _ptr(rot), n_rot,
-                                      n_pose, _ptr(shift), n_sh, _ptr(out), out.shape[2], wp, wb,
+    _call(_LIB.tp_project_3d_to_2d_ws(_ptr(vol), n_rec, Dv, _ptr(rot), n_rot,
+                                      n_pose, _ptr(shift), n_sh, _ptr(out), Do, wp, wb,
                                       _opts(opts), _stream(stream)), "tp_project_3d_to_2d_ws")
 
 
 def tp_project_backward_ws(ndim, rec, rot, shift, grad_out, grad_rec, grad_rot, grad_shift,
                            workspace, opts=None, stream=None):
-    _need(rec, torch.complex64, "rec", ndim + 1)
-    _need(grad_out, torch.complex64, "grad_out", 4)
-    _need(grad_rec, torch.complex64, "grad_rec", ndim + 1)
-    _need(grad_rot, torch.float32, "grad_rot", 4)
-    _need(grad_shift, torch.float32, "grad_shift", 3)
-    n_rot, n_pose, n_sh = _rs(rot, shift, ndim)
+    n_rec, Dv, n_rot, n_pose, n_sh, Do = _backward_checks(ndim, rec, rot, shift, grad_out,
+                                                          grad_rec, grad_rot, grad_shift)
     wp, wb = _ws(workspace)
-    _call(_LIB.tp_project_backward_ws(int(ndim), _ptr(rec), rec.shape[0], rec.shape[1], _ptr(rot),
+    _call(_LIB.tp_project_backward_ws(int(ndim), _ptr(rec), n_rec, Dv, _ptr(rot),
                                       n_rot, n_pose, _ptr(shift), n_sh, _ptr(grad_out),
-                                      grad_out.shape[2], _ptr(grad_rec), _ptr(grad_rot),
+                                      Do, _ptr(grad_rec), _ptr(grad_rot),
                                       _ptr(grad_shift), wp, wb, _opts(opts), _stream(stream)),
           "tp_project_backward_ws")
 
 
 def tp_project_3d_to_2d_noalloc(vol, rot, shift, out, opts=None, stream=None):
-    _need(vol, torch.complex64, "vol", 4)
-    _need(out, torch.complex64, "out", 4)
-    n_rot, n_pose, n_sh = _rs(rot, shift, 3)
-    _call(_LIB.tp_project_3d_to_2d_noalloc(_ptr(vol), vol.shape[0], vol.shape[1], _ptr(rot), n_rot,
-                                           n_pose, _ptr(shift), n_sh, _ptr(out), out.shape[2],
+    n_rec, Dv, n_rot, n_pose, n_sh, Do = _project_checks(3, vol, rot, shift, out, "vol")
+    _call(_LIB.tp_project_3d_to_2d_noalloc(_ptr(vol), n_rec, Dv, _ptr(rot), n_rot,
+                                           n_pose, _ptr(shift), n_sh, _ptr(out), Do,
                                            _opts(opts), _stream(stream)),
           "tp_project_3d_to_2d_noalloc")
 
 
 def tp_pad_volume(ndim, vol, factor, out, stream=None):
-    _need(vol, torch.float32, "vol", ndim + 1)
-    _need(out, torch.float32, "out", ndim + 1)
-    _call(_LIB.tp_pad_volume(int(ndim), _ptr(vol), vol.shape[0], vol.shape[-1], int(factor),
+    n, D, P = _sz(vol, 0), _sz(vol, ndim), int(factor) * _sz(vol, ndim)
+    _check((vol, torch.float32, "vol", (n,) + (D,) * ndim),
+           (out, torch.float32, "out", (n,) + (P,) * ndim))
+    _call(_LIB.tp_pad_volume(int(ndim), _ptr(vol), n, D, int(factor),
                              _ptr(out), _stream(stream)), "tp_pad_volume")
 
 
 def tp_crop_volume(ndim, padded, factor, out, stream=None):
-    _need(padded, torch.float32, "padded", ndim + 1)
-    _need(out, torch.float32, "out", ndim + 1)
-    _call(_LIB.tp_crop_volume(int(ndim), _ptr(padded), out.shape[0], out.shape[-1], int(factor),
+    n, D, P = _sz(out, 0), _sz(out, ndim), int(factor) * _sz(out, ndim)
+    _check((padded, torch.float32, "padded", (n,) + (P,) * ndim),
+           (out, torch.float32, "out", (n,) + (D,) * ndim))
+    _call(_LIB.tp_crop_volume(int(ndim), _ptr(padded), n, D, int(factor),
                               _ptr(out), _stream(stream)), "tp_crop_volume")
 
 

@@ -175,3 +175,96 @@ def test_binding_rejects_bad_tensors():
         tp.tp_project_3d_to_2d(vol, rot, None, out)          # CPU tensors
     with pytest.raises(TypeError):
         tp.tp_project_3d_to_2d(vol.real.contiguous(), rot, None, out)
+
+
+def _z(shape, complex_=False):
+    import torch
+    return torch.zeros(shape, dtype=torch.complex64 if complex_ else torch.float32)
+
+
+def test_binding_checks_every_shape_before_the_device():
+    """The binding passes sizes taken from some tensors' shapes; every other tensor must
+    agree with them exactly, or the kernels would index past it.  A disagreeing shape is a
+    ValueError on any device; consistent CPU tensors get as far as the device check."""
+    vol, rot, sh, out = _z((2, 8, 8, 5), True), _z((2, 3, 3, 3)), _z((1, 3, 2)), _z((2, 3, 8, 5), True)
+    with pytest.raises(TypeError, match="CUDA"):
+        tp.tp_project_3d_to_2d(vol, rot, sh, out)
+    for bad in [dict(out=_z((2, 2, 8, 5), True)),            # pose count
+                dict(out=_z((1, 3, 8, 5), True)),            # reconstruction count
+                dict(out=_z((2, 3, 8, 4), True)),            # half axis of the image
+                dict(vol=_z((2, 8, 8, 4), True)),            # half axis of the volume
+                dict(vol=_z((2, 8, 6, 5), True)),            # not a cube
+                dict(rot=_z((2, 3, 3, 2))),                  # matrix shape
+                dict(sh=_z((1, 2, 2))),                      # shifts for fewer poses
+                dict(sh=_z((1, 3, 3))),                      # three shift components
+                dict(sh=_z((3,)))]:                          # wrong rank
+        a = {**dict(vol=vol, rot=rot, sh=sh, out=out), **bad}
+        with pytest.raises(ValueError, match="must have shape"):
+            tp.tp_project_3d_to_2d(a["vol"], a["rot"], a["sh"], a["out"])
+        with pytest.raises(ValueError, match="must have shape"):
+            tp.tp_project_3d_to_2d_ws(a["vol"], a["rot"], a["sh"], a["out"], None)
+        with pytest.raises(ValueError, match="must have shape"):
+            tp.tp_project_3d_to_2d_noalloc(a["vol"], a["rot"], a["sh"], a["out"])
+    # 2D: images [n_rec][D][D/2+1], rotations 2 x 2
+    img, rot2 = _z((2, 8, 5), True), _z((2, 3, 2, 2))
+    with pytest.raises(TypeError, match="CUDA"):
+        tp.tp_project_2d_to_2d(img, rot2, sh, out)
+    with pytest.raises(ValueError, match="must have shape"):
+        tp.tp_project_2d_to_2d(img, rot, sh, out)            # 3 x 3 matrices
+    # backward: gradients shaped like their inputs; the shift gradient [1][n_pose][2] without shift
+    gR, gS1 = _z((2, 3, 3, 3)), _z((1, 3, 2))
+    with pytest.raises(TypeError, match="CUDA"):
+        tp.tp_project_backward(3, vol, rot, None, out, vol, gR, gS1)
+    for args in [(vol, rot, None, out, _z((2, 8, 8, 4), True), gR, gS1),
+                 (vol, rot, None, out, vol, _z((1, 3, 3, 3)), gS1),
+                 (vol, rot, None, out, vol, gR, _z((2, 3, 2))),
+                 (vol, rot, sh, _z((2, 3, 8, 4), True), vol, gR, gS1)]:
+        with pytest.raises(ValueError, match="must have shape"):
+            tp.tp_project_backward(3, *args)
+        with pytest.raises(ValueError, match="must have shape"):
+            tp.tp_project_backward_ws(3, *args, None)
+
+
+def test_binding_checks_insertion_and_padding_shapes():
+    proj, w = _z((2, 3, 8, 5), True), _z((2, 3, 8, 5))
+    rot = _z((1, 3, 3, 3))
+    vol, wvol = _z((2, 12, 12, 7), True), _z((2, 12, 12, 7))
+    with pytest.raises(TypeError, match="CUDA"):
+        tp.tp_backproject_2d_to_3d(proj, w, rot, None, vol, wvol, 12)
+    with pytest.raises(TypeError, match="CUDA"):                 # weights only: no data image
+        tp.tp_backproject_2d_to_3d(None, w, rot, None, None, wvol, 12)
+    for args in [(proj, _z((2, 3, 8, 4)), rot, None, vol, wvol, 12),
+                 (proj, w, rot, None, vol, wvol, 10),             # Dv disagrees with the outputs
+                 (proj, w, rot, None, vol, _z((1, 12, 12, 7)), 12),
+                 (proj, w, _z((1, 2, 3, 3)), None, vol, wvol, 12)]:
+        with pytest.raises(ValueError, match="must have shape"):
+            tp.tp_backproject_2d_to_3d(*args)
+    img, wimg = _z((2, 12, 7), True), _z((2, 12, 7))
+    rot2 = _z((2, 3, 2, 2))
+    with pytest.raises(TypeError, match="CUDA"):
+        tp.tp_backproject_2d_to_2d(proj, w, rot2, None, img, wimg, 12)
+    with pytest.raises(ValueError, match="must have shape"):
+        tp.tp_backproject_2d_to_2d(proj, w, rot2, None, vol, wimg, 12)
+    # backward of the insertion
+    gR = _z((1, 3, 3, 3))
+    with pytest.raises(TypeError, match="CUDA"):
+        tp.tp_backproject_backward(3, proj, w, rot, None, vol, wvol, proj, w, gR, None)
+    with pytest.raises(ValueError, match="must have shape"):
+        tp.tp_backproject_backward(3, proj, w, rot, None, vol, _z((2, 12, 12, 6)), proj, w, gR, None)
+    with pytest.raises(ValueError, match="must have shape"):
+        tp.tp_backproject_backward(3, proj, w, rot, None, vol, wvol, _z((2, 4, 8, 5), True), w, gR,
+                                   None)
+    with pytest.raises(ValueError, match="image size"):
+        tp.tp_backproject_backward(3, None, None, rot, None, vol, wvol, None, None, gR, None)
+    # padding: out is factor * D on every axis, and the adjoint the other way round
+    v, X = _z((1, 6, 6, 6)), _z((1, 12, 12, 12))
+    with pytest.raises(TypeError, match="CUDA"):
+        tp.tp_pad_volume(3, v, 2, X)
+    with pytest.raises(TypeError, match="CUDA"):
+        tp.tp_crop_volume(3, X, 2, v)
+    with pytest.raises(ValueError, match="must have shape"):
+        tp.tp_pad_volume(3, v, 2, _z((1, 12, 12, 10)))
+    with pytest.raises(ValueError, match="must have shape"):
+        tp.tp_crop_volume(3, _z((1, 12, 12, 12)), 3, v)
+    with pytest.raises(ValueError, match="must have shape"):
+        tp.tp_pad_volume(2, _z((1, 6, 5)), 2, _z((1, 12, 10)))
