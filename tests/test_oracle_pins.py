@@ -316,6 +316,9 @@ CASES = [
     (3, 0, 0, 1.0, 8, 8, 100.0, False, 2, 1),
     (2, 1, 1, 1.0, 12, 12, -1.0, True, 3, 3),
     (2, 0, 0, 1.5, 12, 8, 3.5, True, 2, 1),
+    # image boxes larger than the volume: samples beyond the stored range read zero
+    (3, 1, 1, 1.0, 8, 14, -1.0, True, 1, 1),
+    (2, 0, 0, 1.0, 8, 16, -1.0, True, 2, 2),
 ]
 
 

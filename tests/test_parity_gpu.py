@@ -28,6 +28,12 @@ CASES = [
     (2, 0, 0, 1.0, 30, 30, -1.0, True, 3, 1, 4),
     (2, 1, 0, 1.5, 36, 24, 10.0, False, 4, 4, 2),
     (2, 0, 1, 1.0, 64, 64, 0.0, True, 2, 2, 3),
+    # image boxes larger than the volume (Do > Dv): the outer samples fall outside the stored
+    # range and read zero
+    (3, 1, 1, 1.0, 16, 24, -1.0, True, 1, 1, 7),
+    (3, 0, 0, 1.0, 16, 20, -1.0, True, 2, 2, 5),
+    (2, 1, 1, 1.0, 16, 24, -1.0, True, 3, 3, 2),
+    (2, 0, 0, 1.0, 12, 30, -1.0, True, 2, 1, 3),
 ]
 
 
