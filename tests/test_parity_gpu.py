@@ -330,3 +330,32 @@ def test_large_box_sampled():
     pix = rng.integers(0, D * (D // 2 + 1), 4000)
     ref = oracle.project_samples(3, rec, rot, items, pix, shift, interp=1)
     assert max_rel(y.reshape(3, -1)[items, pix], ref) <= TOL_FWD
+
+
+def test_large_2d_box_fallback_kernels():
+    """2D boxes beyond the shared-memory tables: at D = 4100 the gathers take the per-pixel
+    kernels (image boxes above 4096) and the insertion and image gradient the direct-atomic
+    kernel (boxes above 1024).  Forward on sampled pixels, full backward and insertion with
+    weights against the oracle."""
+    rng = np.random.default_rng(21)
+    D = 4100
+    H = D // 2 + 1
+    rec = crandn32(rng, (2, D, H))
+    rot = rotations(rng, 2, 2).reshape(2, 1, 2, 2)
+    shift = rng.uniform(-40, 40, (2, 1, 2)).astype(np.float32)
+    grad = crandn32(rng, (2, 1, D, H))
+    w = rng.uniform(0.0, 2.0, (2, 1, D, H)).astype(np.float32)
+    op, kw = opts(1), dict(interp=1, layout=1)
+    y = host(tp.project(dev(rec), dev(rot), dev(shift), opts=op))
+    items, pix = rng.integers(0, 2, 4000), rng.integers(0, D * H, 4000)
+    ref = oracle.project_samples(2, rec, rot, items, pix, shift, **kw)
+    assert max_rel(y.reshape(2, -1)[items, pix], ref) <= TOL_FWD
+    g_rec, g_rot, g_sh = tp.project_backward(dev(rec), dev(rot), dev(grad), dev(shift), opts=op)
+    r_rec, r_rot, r_sh = oracle.project_backward(2, rec, rot, grad, shift, **kw)
+    assert max_rel(host(g_rec), r_rec) <= TOL_BWD
+    assert max_rel(host(g_rot), r_rot) <= TOL_BWD
+    assert max_rel(host(g_sh), r_sh) <= TOL_BWD
+    vol, wvol = tp.backproject(dev(grad), dev(rot), dev(shift), dev(w), Dv=D, opts=op, ndim=2)
+    r_vol, r_w = oracle.backproject(2, grad, rot, weights=w, shift=shift, Dv=D, **kw)
+    assert max_rel(host(vol), r_vol) <= TOL_BWD
+    assert max_rel(host(wvol), r_w) <= TOL_BWD
