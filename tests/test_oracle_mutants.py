@@ -36,6 +36,13 @@ MUTANTS = {
     "linear_derivative_sign": ("if (d >= 0.0 && d < 1.0) return -1.0;", "if (d >= 0.0 && d < 1.0) return 1.0;"),
     "cubic_derivative_outer": ("return s * (3.0 * a * u * u - 10.0 * a * u + 8.0 * a);",
                                "return s * (3.0 * a * u * u - 10.0 * a * u + 7.0 * a);"),
+    "x0_plane_mirrored": ("*mirror = tx < 0;", "*mirror = tx <= 0;"),
+    "mirror_keeps_z": ("        tz = -tz;\n    }", "    }"),
+    "shift_axes_swapped": ("(double)px.kx * s[0] + (double)px.ky * s[1]",
+                           "(double)px.kx * s[1] + (double)px.ky * s[0]"),
+    "fftw_nyquist_row_positive": ("return i < D / 2 ? i : i - D;", "return i <= D / 2 ? i : i - D;"),
+    "default_cutoff_uses_rec_box": ("cutoff = cutoff < 0.0 ? 0.5 * Do : cutoff;",
+                                    "cutoff = cutoff < 0.0 ? 0.5 * Dv : cutoff;"),
 }
 
 

@@ -184,6 +184,26 @@ def test_identity_projection_is_central_plane_everywhere(orc):
         assert np.all(out[~keep] == 0)
 
 
+@pytest.mark.parametrize("ndim,Dv,Do,o", [(3, 48, 32, 1.25), (2, 48, 32, 1.25), (3, 20, 32, 0.5),
+                                          (2, 24, 40, 0.5)])
+def test_default_cutoff_is_the_disk_inscribed_in_the_image(orc, ndim, Dv, Do, o):
+    """Without a cutoff, the sampled pixels are exactly the integer points of the disk of
+    radius Do/2 in the half plane of the image box, whatever the volume's box (smaller or
+    larger than the image).  The disk is enumerated by brute force: 414 points at Do = 32.
+    o keeps every sample of the disk inside the stored band, so each of them is non-zero."""
+    rng = np.random.default_rng(Dv * 100 + Do)
+    H = Dv // 2 + 1
+    V = crandn(rng, (1, Dv, Dv, H) if ndim == 3 else (1, Dv, H))
+    R = random_rotations(rng, 3, ndim)[None]
+    y = orc.project(ndim, V, R, None, Do=Do, interp=1, oversampling=o)
+    disk = np.array([[kx * kx + ky * ky <= (Do // 2) ** 2 for kx in range(Do // 2 + 1)]
+                     for ky in range(-Do // 2, Do // 2)])     # centered rows
+    if Do == 32:
+        assert disk.sum() == 414
+    assert np.all(y[..., ~disk] == 0)
+    assert np.all(y[..., disk] != 0)
+
+
 # ------------------------------------------------------- shift theorem ----
 
 @pytest.mark.parametrize("ndim", [2, 3])
