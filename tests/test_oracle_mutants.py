@@ -43,6 +43,15 @@ MUTANTS = {
     "fftw_nyquist_row_positive": ("return i < D / 2 ? i : i - D;", "return i <= D / 2 ? i : i - D;"),
     "default_cutoff_uses_rec_box": ("cutoff = cutoff < 0.0 ? 0.5 * Do : cutoff;",
                                     "cutoff = cutoff < 0.0 ? 0.5 * Dv : cutoff;"),
+    "grad_rot_drops_oversampling": ("+= g.o * q[b] * creal(conj(gp) * dv[a]);",
+                                    "+= q[b] * creal(conj(gp) * dv[a]);"),
+    "weights_skip_mirrored": ("if (W) W[off] += w * wt;", "if (W && !mirror) W[off] += w * wt;"),
+    "linear_tent_curved": ("return u < 1.0 ? 1.0 - u : 0.0;", "return u < 1.0 ? 1.0 - u * u : 0.0;"),
+    "dv_z_conjugated": ("dv[2] += dwz[a] * wy[b] * wx[k] * val;",
+                        "dv[2] += dwz[a] * wy[b] * wx[k] * conj(val);"),
+    "cubic_inner_perturbed": ("if (u <= 1.0) return (a + 2.0) * u * u * u - (a + 3.0) * u * u + 1.0;",
+                              "if (u <= 1.0) return (a + 2.0) * u * u * u - (a + 3.0) * u * u + 1.0"
+                              " + 0.01 * u * (1.0 - u);"),
 }
 
 

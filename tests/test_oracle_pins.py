@@ -432,10 +432,12 @@ def _coords_clear_of_integers(R, Do, o, margin=1e-4):
     return True
 
 
-@pytest.mark.parametrize("ndim,interp,n_rec,n_rot", [(3, 1, 1, 1), (3, 0, 1, 1), (3, 1, 2, 1),
-                                                     (2, 1, 2, 2), (2, 0, 1, 1)])
-def test_rotation_and_shift_gradients_match_central_differences(orc, ndim, interp, n_rec, n_rot):
-    D, n_pose, o = 10, 3, 1.0
+@pytest.mark.parametrize("ndim,interp,n_rec,n_rot,o", [(3, 1, 1, 1, 1.0), (3, 0, 1, 1, 1.0),
+                                                       (3, 1, 2, 1, 1.0), (2, 1, 2, 2, 1.0),
+                                                       (2, 0, 1, 1, 1.0), (3, 1, 1, 1, 1.5),
+                                                       (2, 0, 2, 1, 0.75)])
+def test_rotation_and_shift_gradients_match_central_differences(orc, ndim, interp, n_rec, n_rot, o):
+    D, n_pose = 10, 3
     H = D // 2 + 1
     seed = 20
     while True:
