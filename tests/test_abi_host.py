@@ -268,3 +268,38 @@ def test_binding_checks_insertion_and_padding_shapes():
         tp.tp_crop_volume(3, _z((1, 12, 12, 12)), 3, v)
     with pytest.raises(ValueError, match="must have shape"):
         tp.tp_pad_volume(2, _z((1, 6, 5)), 2, _z((1, 12, 10)))
+
+
+def test_header_is_plain_c_and_links(tmp_path):
+    """include/tp.h compiles as strict C99 and a C program links against libtp.so with every
+    declared function referenced; the calls it makes return before any CUDA call (argument
+    validation, status strings, workspace sizes), so no GPU is needed."""
+    import os
+
+    pkg = os.path.dirname(tp.LIB_PATH)
+    refs = ",\n    ".join(f"(void (*)(void)){name}" for name in tp.header_symbols())
+    (tmp_path / "t.c").write_text(f"""#include <stdio.h>
+#include "tp.h"
+static void (*const every_entry[])(void) = {{
+    {refs}
+}};
+int main(void) {{
+    tp_opts o = {{TP_CUBIC, TP_LAYOUT_CENTERED, 1.0f, -1.0f}};
+    printf("%s\\n", tp_status_string(TP_ERR_SHAPE));
+    printf("%d\\n", (int)tp_project_3d_to_2d(NULL, 1, 7, NULL, 1, 1, NULL, 1, NULL, 8, &o, NULL));
+    printf("%d\\n", (int)tp_project_2d_to_2d(NULL, 1, 8, NULL, 1, 1, NULL, 1, NULL, 8, NULL, NULL));
+    printf("%zu\\n", tp_workspace_size(3, 1, 128, &o));
+    printf("%d\\n", (int)(sizeof every_entry / sizeof every_entry[0]));
+    return 0;
+}}
+""")
+    exe = tmp_path / "t"
+    subprocess.run(["gcc", "-std=c99", "-Wall", "-Wextra", "-Werror", "-pedantic",
+                    "-I", os.path.join(os.path.dirname(pkg), "include"), str(tmp_path / "t.c"),
+                    "-L", pkg, "-ltp", f"-Wl,-rpath,{pkg}", "-o", str(exe)], check=True)
+    out = subprocess.run([str(exe)], capture_output=True, text=True, check=True).stdout.split("\n")
+    assert out[0].startswith("TP_ERR_SHAPE")
+    assert out[1] == "2"                    # odd volume box
+    assert out[2] == "1"                    # valid sizes, one item, NULL pointers: TP_ERR_NULL
+    assert out[3] == str(128 * 128 * 65 * 4 * 8)
+    assert out[4] == str(len(tp.header_symbols()))
