@@ -150,9 +150,10 @@ tp_status tp_project_backward(int ndim, const void* rec, int n_rec, int Dv, cons
  *
  * tp_workspace_size returns the bytes needed (n_rec * Dv * Dv * (Dv/2+1) * NT * 8), or 0
  * when the workspace would not be used (ndim = 2, invalid sizes or options, or NT times one
- * volume's elements >= 2^31).  workspace = NULL, or a size of 0, runs the plain path.
- * Errors, in addition to the plain call's: TP_ERR_SHAPE when workspace_bytes is below the
- * size needed, TP_ERR_VALUE when the workspace is not 32-byte aligned.  The workspace must
+ * volume's elements >= 2^31).  A NULL workspace runs the plain path; so does any workspace
+ * when tp_workspace_size is 0 for these arguments (the workspace is then ignored).
+ * Errors, in addition to the plain call's: TP_ERR_SHAPE when a non-NULL workspace is
+ * smaller than tp_workspace_size, TP_ERR_VALUE when it is not 32-byte aligned.  The workspace must
  * not overlap any argument; its contents are scratch (undefined after the call), and two
  * calls in flight at once need two workspaces. */
 size_t tp_workspace_size(int ndim, int n_rec, int Dv, const tp_opts* opts);
