@@ -100,7 +100,11 @@ def test_rot2d_d256_cubic_full_sampled_images():
     assert max_rel(host(g_sh[ti]), r_sh) <= TOL_BWD
 
 
-def _fwdbwd3d_sampled(name, n_pix=6000, n_poses=48):
+def _fwdbwd3d_sampled(name, n_pix=6000, n_poses=48, n_sub=None):
+    """n_sub: None compares the whole volume gradient of the full batch with the oracle;
+    an integer compares the whole volume gradient of the first n_sub poses of every
+    reconstruction (the same kernel and launch shape on a batch the oracle finishes in
+    seconds)."""
     wl = synth.make_workload(name)
     V, R, S, G = dev(wl.rec), dev(wl.rot), dev(wl.shift), dev(wl.grad)
     op = wl_opts(wl)
@@ -130,7 +134,21 @@ def _fwdbwd3d_sampled(name, n_pix=6000, n_poses=48):
     tpo = torch.from_numpy(poses).cuda()
     assert max_rel(host(g_rot[:, tpo]), r_rot) <= TOL_BWD
     assert max_rel(host(g_sh[:, tpo]), r_sh) <= TOL_BWD
-    # the volume gradient through the adjoint identity
+    # the volume gradient voxel by voxel against the oracle, over every voxel of the box
+    if n_sub is None:
+        r_rec, _, _ = oracle.project_backward(3, wl.rec, wl.rot, wl.grad, wl.shift,
+                                              want_rot=False, want_shift=False, **kw)
+        assert max_rel(host(g_rec), r_rec) <= TOL_BWD
+    else:
+        idx = np.arange(n_sub)
+        g_sub = torch.empty_like(V)
+        sl = lambda t: t[:, :n_sub].contiguous()  # noqa: E731
+        tp.tp_project_backward(3, V, sl(R), sl(S), sl(G), g_sub, None, None, op)
+        r_rec, _, _ = oracle.project_backward(3, wl.rec, sub(wl.rot, idx), sub(wl.grad, idx),
+                                              sub(wl.shift, idx), want_rot=False,
+                                              want_shift=False, **kw)
+        assert max_rel(host(g_sub), r_rec) <= TOL_BWD
+    # and the full batch's volume gradient through the adjoint identity
     Vr = dev(crandn32(rng, wl.rec.shape))
     PV = tp.project(Vr, R, S, opts=op)
     assert adjoint_gap(PV, G, Vr, g_rec) <= 1e-5
@@ -147,7 +165,7 @@ def test_fwdbwd3d_d128_cubic_r8_full_sampled():
 
 
 def test_fwdbwd3d_d256_cubic_full_sampled():
-    _fwdbwd3d_sampled("fwdbwd3d_d256_cubic_b50000", n_pix=4000, n_poses=24)
+    _fwdbwd3d_sampled("fwdbwd3d_d256_cubic_b50000", n_pix=4000, n_poses=24, n_sub=256)
 
 
 def test_chunked_volume_gradient_equals_the_backward():
