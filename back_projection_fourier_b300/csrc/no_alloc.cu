@@ -23,8 +23,10 @@ constexpr int kMaxDevices = 64;
 std::mutex g_mutex;
 void* g_scratch_addr[kMaxDevices] = {};
 
-// Device address of g_scratch on the current device, looked up once per device.  In host
-// code the name g_scratch is only a host-side stand-in, never a device address.
+// Device address of g_scratch on the current device, looked up once per device ordinal for
+// the life of the process (a cudaDeviceReset would unload the array; the header tells
+// callers not to use this entry point on a device they have reset).  In host code the name
+// g_scratch is only a host-side stand-in, never a device address.
 tp_status scratch_address(void** out)
 {
     int dev = -1;

@@ -179,8 +179,12 @@ tp_status tp_project_backward_ws(int ndim, const void* rec, int n_rec, int Dv, c
  *   that the library holds in device memory on every GPU that loads it, until the process
  *   exits.  Sizes whose grouped copy needs more (tp_workspace_size above 34078720) return
  *   TP_ERR_SHAPE before anything is enqueued.  The call allocates nothing.
- *   The first call on a device looks up the array's device address (cudaGetSymbolAddress)
- *   and keeps it for the later calls.
+ *   The first call on a device, with that device current, looks up the array's device
+ *   address (cudaGetSymbolAddress) and keeps it, per process and per device ordinal, for
+ *   the later calls.  Make that first call on each device before any stream capture.  The
+ *   address is not looked up again after a cudaDeviceReset (which unloads the library's
+ *   device code and with it the array), so a process must not call this entry point on a
+ *   device it has reset.
  *   All calls share the one array and each overwrites what it reads, so calls whose work
  *   overlaps on the GPU (other streams, other host threads) race and must be ordered by
  *   the caller. */
