@@ -175,13 +175,26 @@ WORKLOADS = {
 
 
 def make_workload(name: str, B: int | None = None, interp: int | None = None,
-                  with_grad: bool = True, layout: int = CENTERED) -> Workload:
-    """Draw the inputs of a named workload; ``B`` overrides the batch (same recipe)."""
+                  with_grad: bool = True, layout: int = CENTERED,
+                  poses: tuple[int, int] | None = None) -> Workload:
+    """Draw the inputs of a named workload; ``B`` overrides the batch (same recipe).
+
+    ``poses = (a, b)`` keeps only poses a..b-1 of every reconstruction (3D workloads): the
+    rotations, shifts, upstream gradients and weights of those poses, drawn exactly as in
+    the whole batch (the per-item arrays regenerate those items alone), and ``B`` becomes
+    the number of projections kept.  This is how one rank of a data-parallel run draws its
+    shard of a larger batch without drawing the rest."""
     number, ndim, op, interp0, D, B0, rc, amp, falloff, *rest = WORKLOADS[name]
     n_rec = rest[0] if rest else 1
     B = B0 if B is None else B
     if B % n_rec:
         raise ValueError(f"batch {B} is not a multiple of the {n_rec} reconstructions")
+    if poses is not None:
+        if ndim != 3:
+            raise ValueError("pose ranges apply to 3D workloads (2D items are images)")
+        a, b = poses
+        if not 0 <= a <= b <= B // n_rec:
+            raise ValueError(f"pose range {poses} outside 0..{B // n_rec}")
     interp = interp0 if interp is None else interp
     seed = 1000 + number
     rng = np.random.default_rng(seed)
@@ -199,7 +212,7 @@ def make_workload(name: str, B: int | None = None, interp: int | None = None,
     if amp > 0:
         s = shifts(rng, B, amp)
         wl.shift = s.reshape(n_rec, B // n_rec, 2) if ndim == 3 else s[:, None]
-    if op == "insert" or (op == "fwdbwd" and with_grad):
+    if (op == "insert" or (op == "fwdbwd" and with_grad)) and poses is None:
         g = cn01_items(seed, 1, B, (D, H))
         wl.grad = g.reshape(n_rec, B // n_rec, D, H) if ndim == 3 else g[:, None]
     if op == "insert":
@@ -207,4 +220,18 @@ def make_workload(name: str, B: int | None = None, interp: int | None = None,
         wl.weights = np.broadcast_to(w, (wl.n_rec, wl.n_pose, D, H))
     wl.extra["shift_amp"] = amp
     wl.extra["falloff"] = falloff
+    if poses is not None:
+        a, b = poses
+        n_pose = B // n_rec
+        keep = lambda x: None if x is None else np.ascontiguousarray(x[:, a:b])  # noqa: E731
+        wl.rot, wl.shift = keep(wl.rot), keep(wl.shift)
+        if wl.weights is not None:
+            wl.weights = np.broadcast_to(wl.weights[:1, :1], (n_rec, b - a, D, H))
+        if op == "insert" or (op == "fwdbwd" and with_grad):
+            items = (np.arange(n_rec)[:, None] * n_pose + np.arange(a, b)[None, :]).ravel()
+            wl.grad = cn01_items(seed, 1, B, (D, H), items).reshape(n_rec, b - a, D, H)
+        wl.n_pose = b - a
+        wl.B = n_rec * (b - a)
+        wl.extra["poses"] = (a, b)
+        wl.extra["batch_total"] = B
     return wl
