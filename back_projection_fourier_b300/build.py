@@ -16,6 +16,9 @@ CSRC = PKG / "csrc"
 LIB = PKG / "libtp.so"
 INCLUDE = PKG.parent / "include"
 SOURCES = ["kernels.cu", "pad.cu", "tp_abi.cu", "no_alloc.cu"]
+# microbenchmarks of the on-chip units (include/tp_peaks.h), a library of their own
+PEAKS_LIB = PKG / "libtp_peaks.so"
+PEAKS_SOURCES = ["peaks.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 
@@ -38,18 +41,26 @@ def stale() -> bool:
     return any(p.stat().st_mtime > t for p in _inputs())
 
 
-def build(force: bool = False, verbose: bool = False) -> Path:
-    """Compile every CUDA source of the package into libtp.so (no-op when up to date)."""
-    if not force and not stale():
-        return LIB
-    tmp = LIB.with_name(f"libtp.so.{os.getpid()}")
+def _compile(lib: Path, sources, verbose: bool) -> None:
+    tmp = lib.with_name(f"{lib.name}.{os.getpid()}")
     cmd = [nvcc(), *ARCH, "-O3", "-lineinfo", "-std=c++17", "-shared", "-Xcompiler", "-fPIC",
            "-I", str(INCLUDE), "-o", str(tmp)]
     if verbose:
         cmd += ["-Xptxas", "-v"]
-    cmd += [str(CSRC / s) for s in SOURCES]
+    cmd += [str(CSRC / s) for s in sources]
     subprocess.run(cmd, check=True)
-    os.replace(tmp, LIB)
+    os.replace(tmp, lib)
+
+
+def build(force: bool = False, verbose: bool = False) -> Path:
+    """Compile every CUDA source of the package: libtp.so and the microbenchmarks'
+    libtp_peaks.so (each a no-op when up to date)."""
+    if force or stale():
+        _compile(LIB, SOURCES, verbose)
+    peak_inputs = [CSRC / s for s in PEAKS_SOURCES] + [INCLUDE / "tp_peaks.h"]
+    if force or not PEAKS_LIB.exists() or any(
+            p.stat().st_mtime > PEAKS_LIB.stat().st_mtime for p in peak_inputs):
+        _compile(PEAKS_LIB, PEAKS_SOURCES, verbose)
     return LIB
 
 

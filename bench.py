@@ -155,13 +155,14 @@ def run_reference(args, wl):
         oracle_rate(wl, per_step, nthreads)
     dt = time.perf_counter() - t0
     value = items * args.steps / dt
-    sample = f"{items} of {wl.B} projections per step ({wl.op}, fp64)"
+    sample = (f"each timed step is the first {items} of the workload's {wl.B} projections "
+              f"({wl.op}, fp64); ms_per_step is that step's own time")
     line = {
         "impl": "reference", "metric": metric_for(wl), "value": value, "unit": "projections/s",
         "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
-        "ms_per_step": 1e3 * dt / args.steps * (wl.B / items),
+        "ms_per_step": 1e3 * dt / args.steps, "items_per_step": items,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
-        "data": "synthetic", "config": workload_config(wl, "n/a (host oracle)"),
+        "data": "synthetic", "config": workload_config(wl, l2_policy(wl)[1]),
         "cpu_baseline": {"value": value, "unit": "projections/s", "cores": nthreads,
                          "kind": "oracle", "sample": sample},
         "e2e": {"value": value, "unit": "projections/s", "h2d_bytes_per_step": 0,
@@ -225,8 +226,28 @@ class ClockSampler:
 
 # ------------------------------------------------------------------ ours ----
 
+def l2_policy(wl) -> tuple[bool, str]:
+    """(flush, note): inputs smaller than twice the 126 MB L2 get a 256 MB write between timed
+    steps; larger ones stream through L2 anyway.  Both arms state the same policy for a
+    workload, so that their config dicts are equal."""
+    img = wl.D * wl.H * 8
+    if wl.op == "insert":
+        step = wl.B * img * 3 // 2
+    elif wl.op == "fwd":
+        step = wl.B * img
+    else:
+        step = 2 * wl.B * img
+    step += (wl.rec.nbytes if wl.rec is not None else 0)
+    if step < (256 << 20):
+        return True, "L2 flushed between steps (256 MB write; step time = sum of the calls' events)"
+    return False, (f"inputs larger than L2 ({wl.B * img / 1e9:.2f} GB of images read or written "
+                   f"per kernel); no flush")
+
+
 def workload_config(wl, l2: str) -> dict:
-    return {"workload": wl.name, "D": wl.D, "batch": wl.B, "n_rec": wl.n_rec,
+    world = dist_env()[0]
+    par = "dp1" if world == 1 else f"dp{world} (pose shards of {wl.B} per rank, one volume all-reduce)"
+    return {"workload": wl.name, "D": wl.D, "batch": wl.B, "n_rec": wl.n_rec, "parallelism": par,
             "interp": "cubic" if wl.interp else "linear",
             "cutoff": wl.rc, "shift_amp": wl.extra["shift_amp"],
             "layout": "centered" if wl.layout else "fftw", "step": "forward + fused backward",
@@ -246,6 +267,75 @@ def hbm_bytes(wl):
     return {"forward": wl.B * (img + pose) + vol,
             "grad_pose": wl.B * (img + 2 * pose) + vol,
             "grad_volume": wl.B * (img + pose) + vol}
+
+
+def measure_peaks(dev) -> dict | None:
+    """The microbenchmarks of libtp_peaks.so on `dev` (None if that library is missing)."""
+    try:
+        from back_projection_fourier_b300 import peaks
+    except ImportError:
+        return None
+    return peaks.measure(dev)
+
+
+def onchip_work(wl) -> dict:
+    """Algorithmic on-chip work per launch of each kernel of the step.  Taps = kept pixels x
+    (4^3 cubic, 2^3 linear).  Gathers: 8 B per tap read, in rows of 4 (cubic) / 2 (linear)
+    consecutive taps; the forward needs 2 FMA per tap (complex value x real weight), the
+    pose gradients 8 (value and three coordinate derivatives).  Scatter: one float2
+    read-modify-write and 2 FMA per tap."""
+    nt = 4 if wl.interp else 2
+    taps = kept_pixels(wl) * wl.B * nt ** wl.ndim
+    gather = {"taps": taps, "bytes": 8 * taps, "rows": taps // nt, "flop": 4 * taps}
+    scatter = {"taps": taps, "rmw": taps, "flop": 4 * taps}
+    # the insertion with weights adds a float read-modify-write per tap: half the shared
+    # bytes of a float2 one, counted as half of one
+    return {"forward": gather, "grad_pose": dict(gather, flop=16 * taps),
+            "grad_volume": scatter, "grad_image": scatter,
+            "insertion": {"taps": taps, "rmw": taps * 3 // 2, "flop": 6 * taps}}
+
+
+def relevant_roofline(wl, kms, hbm, hbm_peak, pk, sm_mhz) -> dict | None:
+    """Per kernel: T_roof = max(HBM bytes / HBM peak, tap bytes / L1 load peak, flops / FP32
+    peak, scatter read-modify-writes / shared-memory read-modify-write peak), every peak
+    measured (HBM by the driver's copy; the rest by the microbenchmarks of this run);
+    frac = T_roof / measured kernel time.  `row_gather_frac` sets the gathers' tap rows
+    against the measured rate of random 32-byte L1 loads (the gathers' access pattern) as
+    context."""
+    if not pk:
+        return None
+    work = onchip_work(wl)
+    out = {}
+    for k, ms in kms.items():
+        w = work.get(k)
+        if w is None:
+            continue
+        t = {"hbm": hbm[k] / (hbm_peak * 1e9),
+             "fp32": w["flop"] / pk["fma"]["ops_per_s"]}
+        if "bytes" in w:
+            t["l1_load"] = w["bytes"] / pk["l1_load"]["bytes_per_s"]
+        if "rmw" in w:
+            t["smem_rmw"] = w["rmw"] / pk["smem_rmw"]["ops_per_s"]
+        bound = max(t, key=t.get)
+        ent = {"bound": bound, "t_roof_ms": 1e3 * t[bound], "kernel_ms": ms,
+               "frac": 1e3 * t[bound] / ms, "t_ms": {u: 1e3 * v for u, v in t.items()}}
+        if "rows" in w:
+            ent["row_gather_frac"] = w["rows"] / pk["l1_gather32"]["ops_per_s"] / (ms * 1e-3)
+        out[k] = ent
+    sms = pk.get("sms")
+    if sm_mhz and sms:
+        hz = sm_mhz * 1e6 * sms
+        out["per_sm_per_clk"] = {"l1_load_B": pk["l1_load"]["bytes_per_s"] / hz,
+                                 "l1_gather32_loads": pk["l1_gather32"]["ops_per_s"] / hz,
+                                 "l1_gather8_loads": pk["l1_gather8"]["ops_per_s"] / hz,
+                                 "smem_rmw": pk["smem_rmw"]["ops_per_s"] / hz,
+                                 "smem_rmw_random": pk["smem_rmw_random"]["ops_per_s"] / hz,
+                                 "smem_red": pk["smem_red"]["ops_per_s"] / hz,
+                                 "l2_red": pk["l2_red"]["ops_per_s"] / hz,
+                                 "fma_flop": pk["fma"]["ops_per_s"] / hz}
+    out["peak_source"] = ("measured in this run: libtp_peaks.so microbenchmarks (CUDA events, best "
+                          "of 3) on the same GPU; HBM: MEASURED_PEAKS.json copy bandwidth")
+    return out
 
 
 def kept_pixels(wl) -> int:
@@ -293,7 +383,7 @@ def run_ours(args, wl):
     torch.cuda.set_device(local)
     if world > 1:
         dist.init_process_group("nccl", device_id=torch.device("cuda", local))
-    from back_projection_fourier_b300 import tp
+    from back_projection_fourier_b300 import shard, tp
 
     dev = torch.device("cuda", local)
     stream = torch.cuda.current_stream(dev)
@@ -312,29 +402,37 @@ def run_ours(args, wl):
 
     # The fused backward is issued as two C-ABI calls (pose gradients, then the volume
     # gradient): the same outputs as one call, but each call is one gather or one scatter,
-    # so CUDA events give every kernel's own duration.
-    def step(ev=None):
-        if ev is not None:
-            ev[0].record(stream)
-        tp.tp_project_3d_to_2d_ws(V, R, S, Y, WS, op, stream)
-        if ev is not None:
-            ev[1].record(stream)
-        tp.tp_project_backward_ws(3, V, R, S, G, None, gR, gS, WS, op, stream)
-        if ev is not None:
-            ev[2].record(stream)
-        tp.tp_project_backward(3, V, R, S, G, gV, None, None, op, stream)
-        if ev is not None:
-            ev[3].record(stream)
-        if world > 1:
-            dist.all_reduce(torch.view_as_real(gV))
+    # so CUDA events give every kernel's own duration.  The step is the package's
+    # data-parallel step: on N ranks each holds its own pose shard and the volume gradient
+    # is summed with one all-reduce (a no-op on one rank).
+    cur_ev = [None]
 
-    # inputs smaller than twice the 126 MB L2 get a 256 MB write between timed steps
-    step_bytes = 2 * G.numel() * 8 + V.numel() * 8
-    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev) if step_bytes < (256 << 20) else None
-    l2_note = ("L2 flushed between steps (256 MB write; step time = sum of the calls' events)"
-               if flush is not None else
-               f"inputs larger than L2 ({G.numel() * 8 / 1e9:.2f} GB upstream grad read and "
-               f"{G.numel() * 8 / 1e9:.2f} GB projections written per step); no flush")
+    def mark(k):
+        if cur_ev[0] is not None:
+            cur_ev[0][k].record(stream)
+
+    def project(V_, R_, S_):
+        mark(0)
+        tp.tp_project_3d_to_2d_ws(V_, R_, S_, Y, WS, op, stream)
+        mark(1)
+        return Y
+
+    def backward(V_, R_, S_, G_):
+        tp.tp_project_backward_ws(3, V_, R_, S_, G_, None, gR, gS, WS, op, stream)
+        mark(2)
+        tp.tp_project_backward(3, V_, R_, S_, G_, gV, None, None, op, stream)
+        mark(3)
+        return gV, gR, gS
+
+    def step(ev=None):
+        cur_ev[0] = ev
+        shard.shard_step(project, backward, V, R, S, G)
+
+    flush_l2, l2_note = l2_policy(wl)
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev) if flush_l2 else None
+
+    # on-chip peaks of this GPU, measured now, before the step (the relevant roofline)
+    onchip_peaks = measure_peaks(dev) if rank == 0 else None
 
     for _ in range(args.warmup):
         step()
@@ -445,8 +543,7 @@ def run_ours(args, wl):
                                            stream)
                 ev_done[c].record(stream)
             ev_read[k].record(stream)
-            if world > 1:
-                dist.all_reduce(torch.view_as_real(b["gV"]))
+            shard.volume_allreduce(b["gV"])
             ev_vol.record(stream)
             with torch.cuda.stream(s_out):
                 for c, (a, bb) in enumerate(bounds):
@@ -509,19 +606,7 @@ def run_ours(args, wl):
             traffic = ent["dram_bytes_per_launch"] * (wl.B / ent["batch"])
     except (OSError, ValueError, KeyError, ZeroDivisionError):
         pass
-    taps = kept_pixels(wl) * wl.B * (64 if wl.interp else 8)
-    onchip_bytes = {"forward": taps * 8, "grad_pose": taps * 8, "grad_volume": taps * 16}
-    sm_mhz = (clocks or {}).get("sm_mhz") or peaks.get("sm_max_mhz", 2032.0)
-    l1_peak = 148 * 128 * sm_mhz * 1e6 / 1e9
-    roofline = {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
-                "frac": achieved / peak, "traffic": traffic, "kernel": dom,
-                "peak_source": peak_src, "kernel_ms": dom_ms}
-    onchip = {k: {"achieved": onchip_bytes[k] / (kms[k] * 1e-3) / 1e9, "peak": l1_peak,
-                  "unit": "GB/s", "frac": onchip_bytes[k] / (kms[k] * 1e-3) / 1e9 / l1_peak}
-              for k in kms}
-    onchip["bound"] = "l1/smem data pipe"
-    onchip["peak_source"] = "derived: 148 SM x 128 B/clk x median SM clock"
-    onchip["bytes"] = "taps x 8 B (gathers) / taps x 16 B (scatter read-modify-write)"
+    relevant = relevant_roofline(wl, kms, hbm, peak, onchip_peaks, (clocks or {}).get("sm_mhz"))
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
@@ -543,7 +628,7 @@ def run_ours(args, wl):
             "config": workload_config(wl, l2_note),
             "gpu_launches": (3 + 2 * (WS is not None)) * args.steps,
             "kernel_ms": kms,
-            "roofline": roofline, "roofline_onchip": onchip,
+            "roofline": roofline, "roofline_relevant": relevant, "peaks_measured": onchip_peaks,
             "cpu_baseline": cpu, "e2e": e2e, "clocks": clocks,
         }
         print(json.dumps(line), flush=True)
@@ -603,8 +688,10 @@ def run_workload(args, wl):
         what = "2D rotation forward + backward"
     else:
         raise SystemExit(f"no timing recipe for workload {wl.name}")
-    step_bytes = sum(hbm.values())
-    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev) if step_bytes < (256 << 20) else None
+    flush_l2, l2_note = l2_policy(wl)
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev) if flush_l2 else None
+    onchip_peaks = measure_peaks(dev)
+    clock_sampler = ClockSampler(None)
     names = list(calls)
     ev = {k: (torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for k in names}
     tot = {k: 0.0 for k in names}
@@ -619,6 +706,7 @@ def run_workload(args, wl):
         if it >= args.warmup:
             for k in names:
                 tot[k] += ev[k][0].elapsed_time(ev[k][1])
+    clocks = clock_sampler.stop()
     kms = {k: v / args.steps for k, v in tot.items()}
     ms_step = sum(kms.values())
     dom = max(kms, key=kms.get)
@@ -634,12 +722,14 @@ def run_workload(args, wl):
         "unit": "projections/s", "n_gpus": 1, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": "f32", "data": "synthetic",
-        "config": dict(workload_config(wl, "L2 flushed between steps (256 MB write)" if flush is not None
-                                       else "inputs larger than L2; no flush"), step=what),
+        "config": dict(workload_config(wl, l2_note), step=what),
         "gpu_launches": launches * args.steps, "kernel_ms": kms,
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                      "frac": achieved / peak, "traffic": None, "kernel": dom,
                      "peak_source": "measured" if peaks.get("hbm_gbs") else "fallback"},
+        "roofline_relevant": relevant_roofline(wl, kms, hbm, peak, onchip_peaks,
+                                               (clocks or {}).get("sm_mhz")),
+        "peaks_measured": onchip_peaks, "clocks": clocks,
     }
     print(json.dumps(line), flush=True)
     return 0
@@ -737,7 +827,14 @@ def main():
         interp = None if args.interp is None else (1 if args.interp == "cubic" else 0)
         return run_reference(args, synth.make_workload(args.workload, interp=interp))
     interp = None if args.interp is None else (1 if args.interp == "cubic" else 0)
-    wl = synth.make_workload(args.workload, B=args.batch, interp=interp)
+    world, rank, _ = dist_env()
+    if world > 1:
+        # weak scaling: rank r draws and runs only its own shard of a batch of
+        # (workload batch) x N poses
+        from back_projection_fourier_b300 import shard
+        wl = shard.workload_shard(args.workload, args.batch, rank, world, interp=interp)
+    else:
+        wl = synth.make_workload(args.workload, B=args.batch, interp=interp)
     if wl.op != "fwdbwd" or wl.ndim != 3:
         return run_workload(args, wl)
     return run_ours(args, wl)

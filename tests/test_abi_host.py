@@ -303,3 +303,45 @@ int main(void) {{
     assert out[2] == "1"                    # valid sizes, one item, NULL pointers: TP_ERR_NULL
     assert out[3] == str(128 * 128 * 65 * 4 * 8)
     assert out[4] == str(len(tp.header_symbols()))
+
+
+def test_peaks_library_exports_and_validates(tmp_path):
+    """libtp_peaks.so (include/tp_peaks.h) exports what its header declares, the header is
+    plain C99, and bad arguments are refused on the host (status 1) before any CUDA call."""
+    import os
+    import re
+
+    from back_projection_fourier_b300 import peaks
+
+    hdr = os.path.join(os.path.dirname(os.path.dirname(tp.LIB_PATH)), "include", "tp_peaks.h")
+    names = sorted(set(re.findall(r"^\s*(?:int|size_t)\s+(tp_peak_\w+)\s*\(", open(hdr).read(), re.M)))
+    assert names == ["tp_peak_run", "tp_peak_scratch_bytes"]
+    dyn = subprocess.run(["nm", "-D", "--defined-only", str(peaks.LIB_PATH)], capture_output=True,
+                         text=True, check=True).stdout
+    exported = {line.split()[-1] for line in dyn.splitlines() if " T " in line}
+    assert set(names) <= exported
+    P = peaks._lib()
+    need = P.tp_peak_scratch_bytes()
+    assert need >= (8 << 20)
+    o, b = ctypes.c_double(), ctypes.c_double()
+    for kind, ptr, size, ctas, iters in [(0, None, need, 1, 1),          # NULL scratch
+                                         (0, FAKE, need - 1, 1, 1),      # too small
+                                         (0, FAKE + 16, need, 1, 1),     # not 256-aligned
+                                         (0, FAKE, need, 0, 1),          # no CTAs
+                                         (0, FAKE, need, 1, 0),          # no iterations
+                                         (99, FAKE, need, 1, 1)]:        # unknown kind
+        assert P.tp_peak_run(kind, ptr, size, ctas, iters, None, ctypes.byref(o), ctypes.byref(b)) == 1
+    pkg = os.path.dirname(peaks.LIB_PATH)
+    (tmp_path / "p.c").write_text("""#include <stdio.h>
+#include "tp_peaks.h"
+int main(void) {
+    double o = 0, b = 0;
+    printf("%d\\n", tp_peak_run(TP_PEAK_FMA, NULL, tp_peak_scratch_bytes(), 1, 1, NULL, &o, &b));
+    return 0;
+}
+""")
+    exe = tmp_path / "p"
+    subprocess.run(["gcc", "-std=c99", "-Wall", "-Wextra", "-Werror", "-pedantic",
+                    "-I", os.path.dirname(hdr), str(tmp_path / "p.c"), "-L", pkg, "-ltp_peaks",
+                    f"-Wl,-rpath,{pkg}", "-o", str(exe)], check=True)
+    assert subprocess.run([str(exe)], capture_output=True, text=True, check=True).stdout == "1\n"
