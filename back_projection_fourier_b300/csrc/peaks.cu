@@ -29,24 +29,28 @@ constexpr size_t kNeed = kSinkOffset + 256;
 __device__ __forceinline__ uint32_t lcg(uint32_t x) { return x * 1664525u + 1013904223u; }
 
 // Coalesced 16-byte loads from the CTA's window: the data pipe's best case (a warp reads
-// 512 contiguous bytes per instruction).
+// 512 contiguous bytes per instruction).  Each round's offset depends on the values the
+// previous round loaded (the window holds zeros, so it always advances by one round), which
+// keeps the compiler from hoisting or merging loads whose addresses repeat every four rounds.
 __global__ void __launch_bounds__(kThreads) l1_load_kernel(const float4* __restrict__ buf, int iters,
                                                            float* sink)
 {
-    const int n4 = kWindowBytes / 16;
+    const int n4 = kWindowBytes / 16;  // 1024 float4; one round reads 1024 of them
     const float4* w = buf + (size_t)(blockIdx.x % kWindows) * n4;
     float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-    int k = threadIdx.x;
+    uint32_t off = threadIdx.x;
     for (int it = 0; it < iters; ++it) {
+        float4 v[4];
+#pragma unroll
+        for (int u = 0; u < 4; ++u) v[u] = __ldg(w + ((off + u * kThreads) & (n4 - 1)));
 #pragma unroll
         for (int u = 0; u < 4; ++u) {
-            const float4 v = __ldg(w + ((k + u * kThreads) & (n4 - 1)));
-            acc.x += v.x;
-            acc.y += v.y;
-            acc.z += v.z;
-            acc.w += v.w;
+            acc.x += v[u].x;
+            acc.y += v[u].y;
+            acc.z += v[u].z;
+            acc.w += v[u].w;
         }
-        k += 4 * kThreads;
+        off += 4 * kThreads + (__float_as_uint(v[3].w) & 16u);
     }
     if (acc.x + acc.y + acc.z + acc.w < 0.f) sink[0] = acc.x;
 }
@@ -85,7 +89,20 @@ __global__ void __launch_bounds__(kThreads) l1_gather_kernel(const float* __rest
 
 // Shared-memory float2 read-modify-writes.  CONFLICT_FREE: a warp touches 32 consecutive
 // float2 (two wavefronts each way), the best case; otherwise every lane a random float2 of
-// its warp's 512-entry region (distinct lanes may collide in banks, as random taps do).
+// its warp's 512-entry region (distinct lanes may collide in banks, as random taps do).  The
+// loads and stores are volatile, so each one reaches shared memory.
+__device__ __forceinline__ float2 lds_v2(uint32_t a)
+{
+    float2 v;
+    asm volatile("ld.shared.v2.f32 {%0,%1}, [%2];" : "=f"(v.x), "=f"(v.y) : "r"(a));
+    return v;
+}
+
+__device__ __forceinline__ void sts_v2(uint32_t a, float2 v)
+{
+    asm volatile("st.shared.v2.f32 [%0], {%1,%2};" ::"r"(a), "f"(v.x), "f"(v.y) : "memory");
+}
+
 template <bool CONFLICT_FREE>
 __global__ void __launch_bounds__(kThreads) smem_rmw_kernel(int iters, float* sink)
 {
@@ -93,6 +110,7 @@ __global__ void __launch_bounds__(kThreads) smem_rmw_kernel(int iters, float* si
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     for (int e = lane; e < kRmwSlots; e += 32) box[warp][e] = make_float2(0.f, 0.f);
     __syncwarp();
+    const uint32_t base = (uint32_t)__cvta_generic_to_shared(&box[warp][0]);
     uint32_t x = lcg(threadIdx.x + 7);
     const float2 v = make_float2(1e-30f * (float)lane, 0.f);
     for (int it = 0; it < iters; ++it) {
@@ -105,10 +123,11 @@ __global__ void __launch_bounds__(kThreads) smem_rmw_kernel(int iters, float* si
                 x = lcg(x);
                 e = (int)((x >> 9) & (kRmwSlots - 1));
             }
-            float2 a = box[warp][e];
-            a.x += v.x;
-            a.y += v.y;
-            box[warp][e] = a;
+            const uint32_t a = base + 8u * (uint32_t)e;
+            float2 c = lds_v2(a);
+            c.x += v.x;
+            c.y += v.y;
+            sts_v2(a, c);
         }
     }
     __syncwarp();

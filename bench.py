@@ -606,6 +606,9 @@ def run_ours(args, wl):
             traffic = ent["dram_bytes_per_launch"] * (wl.B / ent["batch"])
     except (OSError, ValueError, KeyError, ZeroDivisionError):
         pass
+    roofline = {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
+                "frac": achieved / peak, "traffic": traffic, "kernel": dom,
+                "peak_source": peak_src, "kernel_ms": dom_ms}
     relevant = relevant_roofline(wl, kms, hbm, peak, onchip_peaks, (clocks or {}).get("sm_mhz"))
 
     cpu = None

@@ -39,3 +39,26 @@ def test_kernel_hash_ignores_comments_only(tmp_path, monkeypatch):
     assert bench.kernel_hash() == h0
     src.write_text("int f(int x) {\n    return x + 2;\n}\n")
     assert bench.kernel_hash() != h0
+
+
+def test_relevant_roofline_arithmetic():
+    """T_roof of each kernel is the largest of its measured-peak times; frac = T_roof / time.
+    Fake peaks and times, checked by hand: the forward's 6490 x 16 x 64 taps of 8 B at
+    1e13 B/s take 5.3 ms of L1 time against 0.1 ms of FP32 and HBM time."""
+    wl = synth.make_workload(bench.DEFAULT_WORKLOAD, B=16, with_grad=False)
+    taps = 6490 * 16 * 64
+    pk = {"sms": 148, "l1_load": {"bytes_per_s": 1e13}, "l1_gather8": {"ops_per_s": 1e11},
+          "l1_gather32": {"ops_per_s": 2e11}, "smem_rmw": {"ops_per_s": 2e12},
+          "smem_rmw_random": {"ops_per_s": 1e12}, "smem_red": {"ops_per_s": 5e11},
+          "l2_red": {"ops_per_s": 2e11}, "fma": {"ops_per_s": 7e13}}
+    kms = {"forward": 10.0, "grad_pose": 20.0, "grad_volume": 40.0}
+    hbm = bench.hbm_bytes(wl)
+    r = bench.relevant_roofline(wl, kms, hbm, 6400.0, pk, 2000.0)
+    assert r["forward"]["bound"] == "l1_load"
+    assert r["forward"]["t_roof_ms"] == pytest.approx(1e3 * taps * 8 / 1e13)
+    assert r["forward"]["frac"] == pytest.approx(taps * 8 / 1e13 / 10e-3)
+    assert r["forward"]["row_gather_frac"] == pytest.approx(taps / 4 / 2e11 / 10e-3)
+    assert r["grad_volume"]["bound"] == "smem_rmw"
+    assert r["grad_volume"]["t_roof_ms"] == pytest.approx(1e3 * taps / 2e12)
+    assert r["per_sm_per_clk"]["l1_load_B"] == pytest.approx(1e13 / (2000e6 * 148))
+    assert bench.relevant_roofline(wl, kms, hbm, 6400.0, None, 2000.0) is None
