@@ -280,17 +280,21 @@ def measure_peaks(dev) -> dict | None:
 
 def onchip_work(wl) -> dict:
     """Algorithmic on-chip work per launch of each kernel of the step.  Taps = kept pixels x
-    (4^3 cubic, 2^3 linear).  Gathers: 8 B per tap read, in rows of 4 (cubic) / 2 (linear)
-    consecutive taps; the forward needs 2 FMA per tap (complex value x real weight), the
-    pose gradients 8 (value and three coordinate derivatives).  Scatter: one float2
-    read-modify-write and 2 FMA per tap."""
+    (4^3 cubic, 2^3 linear), in rows of 4 (cubic) / 2 (linear) consecutive x taps.
+    Gathers read 8 B per tap.  Separable sums: the forward forms per row a complex sum
+    weighted by the x weights (one complex FMA per tap) and adds it with the y-z weight
+    (one per row): 4 flop per tap + 4 per row.  The pose gradients also form the
+    x-derivative row sum (one more complex FMA per tap) and add value, x-, y- and
+    z-derivative terms per row: 8 flop per tap + 16 per row.  Scatter: one float2
+    read-modify-write and one complex FMA per tap."""
     nt = 4 if wl.interp else 2
     taps = kept_pixels(wl) * wl.B * nt ** wl.ndim
-    gather = {"taps": taps, "bytes": 8 * taps, "rows": taps // nt, "flop": 4 * taps}
+    rows = taps // nt
+    gather = {"taps": taps, "bytes": 8 * taps, "rows": rows, "flop": 4 * taps + 4 * rows}
     scatter = {"taps": taps, "rmw": taps, "flop": 4 * taps}
     # the insertion with weights adds a float read-modify-write per tap: half the shared
     # bytes of a float2 one, counted as half of one
-    return {"forward": gather, "grad_pose": dict(gather, flop=16 * taps),
+    return {"forward": gather, "grad_pose": dict(gather, flop=8 * taps + 16 * rows),
             "grad_volume": scatter, "grad_image": scatter,
             "insertion": {"taps": taps, "rmw": taps * 3 // 2, "flop": 6 * taps}}
 
@@ -369,7 +373,8 @@ def host_link(b, hG, s_in, s_out, h2d, d2h, step_s) -> dict:
         return best
 
     t_in, t_out, t_both = timed(True, False), timed(False, True), timed(True, True)
-    floor_s = t_both * max(h2d / n_in, d2h / n_out)
+    # each direction at its own rate, and the overlapped part at the shared two-way rate
+    floor_s = max(t_in * h2d / n_in, t_out * d2h / n_out, t_both * min(h2d / n_in, d2h / n_out))
     return {"h2d_GBps": n_in / t_in / 1e9, "d2h_GBps": n_out / t_out / 1e9,
             "both_ways_GBps": [n_in / t_both / 1e9, n_out / t_both / 1e9],
             "floor_ms_per_step": 1e3 * floor_s, "frac": floor_s / step_s}
@@ -516,7 +521,7 @@ def run_ours(args, wl):
         sl = lambda t, a, b: None if t is None else t[:, a:b]  # noqa: E731
         n_e2e = [0]
 
-        def e2e_step():
+        def e2e_step(copy_proj):
             k = n_e2e[0] % 2
             n_e2e[0] += 1
             b = bufs[k]
@@ -548,27 +553,46 @@ def run_ours(args, wl):
             with torch.cuda.stream(s_out):
                 for c, (a, bb) in enumerate(bounds):
                     s_out.wait_event(ev_done[c])
-                    b["oY"][:, a:bb].copy_(b["Y"][:, a:bb], non_blocking=True)
+                    if copy_proj:
+                        b["oY"][:, a:bb].copy_(b["Y"][:, a:bb], non_blocking=True)
                     b["ogR"][:, a:bb].copy_(b["gR"][:, a:bb], non_blocking=True)
                     b["ogS"][:, a:bb].copy_(b["gS"][:, a:bb], non_blocking=True)
                 s_out.wait_event(ev_vol)
                 b["ogV"].copy_(b["gV"], non_blocking=True)
                 ev_out[k].record(s_out)
 
-        for _ in range(max(1, args.warmup)):
-            e2e_step()
-        torch.cuda.synchronize()
-        if world > 1:
-            dist.barrier()
-        t0 = time.perf_counter()
-        for _ in range(args.steps):
-            e2e_step()
-        torch.cuda.synchronize()
-        dt = time.perf_counter() - t0
-        if world > 1:
-            t = torch.tensor([dt], device=dev)
-            dist.all_reduce(t, op=dist.ReduceOp.MAX)
-            dt = float(t.item())
+        def timed_e2e(copy_proj):
+            for _ in range(max(1, args.warmup)):
+                e2e_step(copy_proj)
+            torch.cuda.synchronize()
+            if world > 1:
+                dist.barrier()
+            t0 = time.perf_counter()
+            for _ in range(args.steps):
+                e2e_step(copy_proj)
+            torch.cuda.synchronize()
+            dt = time.perf_counter() - t0
+            if world > 1:
+                t = torch.tensor([dt], device=dev)
+                dist.all_reduce(t, op=dist.ReduceOp.MAX)
+                dt = float(t.item())
+            return dt
+
+        h2d = sum(x.numel() * x.element_size() for x in (hV, hR, hG) + ((hS,) if hS is not None else ()))
+        # the step's result is its gradients (volume, rotations, shifts); the projections stay
+        # on the device, where a loss would consume them
+        dt = timed_e2e(False)
+        d2h = sum(bufs[0][n].numel() * bufs[0][n].element_size() for n in ("ogV", "ogR", "ogS"))
+        e2e = {"value": wl.B * world / (dt / args.steps), "unit": "projections/s",
+               "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+               "result_read_back": "volume, rotation and shift gradients"}
+        e2e["host_link"] = host_link(bufs[0], hG, s_in, s_out, h2d, d2h, dt / args.steps)
+        # the same step reading the 1.09 GB of projections back as well
+        dt_all = timed_e2e(True)
+        d2h_all = d2h + bufs[0]["oY"].numel() * bufs[0]["oY"].element_size()
+        e2e["with_projections"] = {
+            "value": wl.B * world / (dt_all / args.steps), "d2h_bytes_per_step": d2h_all,
+            "host_link": host_link(bufs[0], hG, s_in, s_out, h2d, d2h_all, dt_all / args.steps)}
         # both buffer sets ran the same inputs: their host results must agree (the forward
         # exactly, the gradients up to the order of their float sums)
         if n_e2e[0] >= 2:
@@ -578,11 +602,6 @@ def run_ours(args, wl):
             errs = {n: rel(n) for n in ("ogV", "ogR", "ogS")}
             if not torch.equal(h0["oY"], h1["oY"]) or max(errs.values()) > 1e-5:
                 raise RuntimeError(f"e2e buffer sets disagree: {errs}")
-        h2d = sum(x.numel() * x.element_size() for x in (hV, hR, hG) + ((hS,) if hS is not None else ()))
-        d2h = sum(bufs[0][n].numel() * bufs[0][n].element_size() for n in ("oY", "ogV", "ogR", "ogS"))
-        e2e = {"value": wl.B * world / (dt / args.steps), "unit": "projections/s",
-               "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h}
-        e2e["host_link"] = host_link(bufs[0], hG, s_in, s_out, h2d, d2h, dt / args.steps)
 
     # roofline of the dominant kernel
     dom = max(kms, key=kms.get)
