@@ -54,8 +54,10 @@ def parse():
     ap.add_argument("--cpu-sample", type=int, default=16384, help="poses in the oracle sample")
     ap.add_argument("--batch", type=int, default=None,
                     help="override the workload's batch (small cases for profiling only)")
-    ap.add_argument("--e2e-chunks", type=int, default=8,
-                    help="pose chunks of the pipelined end-to-end step (copies overlap kernels)")
+    ap.add_argument("--e2e-chunks", type=int, default=2,
+                    help="pose chunks of the end-to-end step that reads back the gradients")
+    ap.add_argument("--e2e-proj-chunks", type=int, default=8,
+                    help="pose chunks of the end-to-end step that also reads back the projections")
     ap.add_argument("--interp", choices=["linear", "cubic"], default=None,
                     help="override the workload's interpolation (insertion: both are asked for)")
     ap.add_argument("--study", choices=["oversampling"], default=None,
@@ -508,12 +510,8 @@ def run_ours(args, wl):
         # forward, pose gradients, and the chunk's share of the volume gradient, accumulated
         # by the insertion call (the transpose of the projection, the same kernel as the
         # backward's volume gradient).  One reconstruction: chunks are contiguous pose ranges.
-        n_chunk = args.e2e_chunks if wl.n_rec == 1 else 1
-        bounds = [(wl.n_pose * c // n_chunk, wl.n_pose * (c + 1) // n_chunk) for c in range(n_chunk)]
         s_in, s_out = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
         ev_v = torch.cuda.Event()
-        ev_in = [torch.cuda.Event() for _ in bounds]
-        ev_done = [torch.cuda.Event() for _ in bounds]
         ev_vol = torch.cuda.Event()
         # per buffer set: its inputs were last read (kernels done) / its outputs last copied out
         ev_read = [torch.cuda.Event() for _ in bufs]
@@ -521,7 +519,7 @@ def run_ours(args, wl):
         sl = lambda t, a, b: None if t is None else t[:, a:b]  # noqa: E731
         n_e2e = [0]
 
-        def e2e_step(copy_proj):
+        def e2e_step(copy_proj, bounds, ev_in, ev_done):
             k = n_e2e[0] % 2
             n_e2e[0] += 1
             b = bufs[k]
@@ -561,15 +559,19 @@ def run_ours(args, wl):
                 b["ogV"].copy_(b["gV"], non_blocking=True)
                 ev_out[k].record(s_out)
 
-        def timed_e2e(copy_proj):
+        def timed_e2e(copy_proj, n_chunk):
+            n_chunk = max(1, min(n_chunk, wl.n_pose)) if wl.n_rec == 1 else 1
+            bounds = [(wl.n_pose * c // n_chunk, wl.n_pose * (c + 1) // n_chunk) for c in range(n_chunk)]
+            ev_in = [torch.cuda.Event() for _ in bounds]
+            ev_done = [torch.cuda.Event() for _ in bounds]
             for _ in range(max(1, args.warmup)):
-                e2e_step(copy_proj)
+                e2e_step(copy_proj, bounds, ev_in, ev_done)
             torch.cuda.synchronize()
             if world > 1:
                 dist.barrier()
             t0 = time.perf_counter()
             for _ in range(args.steps):
-                e2e_step(copy_proj)
+                e2e_step(copy_proj, bounds, ev_in, ev_done)
             torch.cuda.synchronize()
             dt = time.perf_counter() - t0
             if world > 1:
@@ -581,17 +583,19 @@ def run_ours(args, wl):
         h2d = sum(x.numel() * x.element_size() for x in (hV, hR, hG) + ((hS,) if hS is not None else ()))
         # the step's result is its gradients (volume, rotations, shifts); the projections stay
         # on the device, where a loss would consume them
-        dt = timed_e2e(False)
+        dt = timed_e2e(False, args.e2e_chunks)
         d2h = sum(bufs[0][n].numel() * bufs[0][n].element_size() for n in ("ogV", "ogR", "ogS"))
         e2e = {"value": wl.B * world / (dt / args.steps), "unit": "projections/s",
                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
-               "result_read_back": "volume, rotation and shift gradients"}
+               "result_read_back": "volume, rotation and shift gradients",
+               "pose_chunks": args.e2e_chunks}
         e2e["host_link"] = host_link(bufs[0], hG, s_in, s_out, h2d, d2h, dt / args.steps)
         # the same step reading the 1.09 GB of projections back as well
-        dt_all = timed_e2e(True)
+        dt_all = timed_e2e(True, args.e2e_proj_chunks)
         d2h_all = d2h + bufs[0]["oY"].numel() * bufs[0]["oY"].element_size()
         e2e["with_projections"] = {
             "value": wl.B * world / (dt_all / args.steps), "d2h_bytes_per_step": d2h_all,
+            "pose_chunks": args.e2e_proj_chunks,
             "host_link": host_link(bufs[0], hG, s_in, s_out, h2d, d2h_all, dt_all / args.steps)}
         # both buffer sets ran the same inputs: their host results must agree (the forward
         # exactly, the gradients up to the order of their float sums)
