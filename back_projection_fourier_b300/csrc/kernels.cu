@@ -884,7 +884,18 @@ __global__ void __launch_bounds__(BT) scatter_rows_kernel(
 // oversampling) use direct vector atomics.
 constexpr int kBoxPitch = 12;
 constexpr int kBoxRows = 81;                        // NY * NZ <= 9 * 9
-constexpr int kTileCap = kBoxPitch * kBoxRows;      // voxels of one warp's box
+
+// Box of one warp, by interpolation.  Cubic: pitch 12, up to 81 rows (every 4 x 4 tile at
+// o = 1: floors span at most 3 sqrt(2) + 1 values, plus 3 taps, on each axis).  Linear: the
+// same tile spans at most 6 floors plus 1 tap, so 7 x 7 x 7: pitch 8 and 49 rows, a box of 392
+// voxels instead of 972, which leaves room for twice the resident warps.  Larger tiles (o > 1)
+// take the per-tap path.
+template <int INTERP>
+struct BoxDims {
+    static constexpr int PITCH = INTERP == kCubic ? kBoxPitch : 8;
+    static constexpr int ROWS = INTERP == kCubic ? kBoxRows : 49;
+    static constexpr int CAP = PITCH * ROWS;
+};
 constexpr int kTilePix = 16;                        // 4 x 4 pixels
 
 template <int INTERP>
@@ -916,20 +927,22 @@ __global__ void __launch_bounds__(kThreads) scatter_tile_kernel(
     constexpr int NWARP = kThreads / 32;
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     extern __shared__ __align__(16) unsigned char sm_raw[];
-    // per warp: acc[kTileCap] float2 | wacc[kTileCap] float | records (TR::WORDS words)
-    float2* acc = reinterpret_cast<float2*>(sm_raw) + warp * (DATA ? kTileCap : 0);
-    float* wacc = reinterpret_cast<float*>(reinterpret_cast<float2*>(sm_raw) + NWARP * (DATA ? kTileCap : 0)) +
-                  warp * (WTS ? kTileCap : 0);
-    float* recf = reinterpret_cast<float*>(reinterpret_cast<float2*>(sm_raw) + NWARP * (DATA ? kTileCap : 0)) +
-                  NWARP * (WTS ? kTileCap : 0) + warp * TR::WORDS;
+    using BX = BoxDims<INTERP>;
+    constexpr int CAP = BX::CAP, PITCH = BX::PITCH, ROWS = BX::ROWS;
+    // per warp: acc[CAP] float2 | wacc[CAP] float | records (TR::WORDS words)
+    float2* acc = reinterpret_cast<float2*>(sm_raw) + warp * (DATA ? CAP : 0);
+    float* wacc = reinterpret_cast<float*>(reinterpret_cast<float2*>(sm_raw) + NWARP * (DATA ? CAP : 0)) +
+                  warp * (WTS ? CAP : 0);
+    float* recf = reinterpret_cast<float*>(reinterpret_cast<float2*>(sm_raw) + NWARP * (DATA ? CAP : 0)) +
+                  NWARP * (WTS ? CAP : 0) + warp * TR::WORDS;
     int* reci = reinterpret_cast<int*>(recf);
-    static_assert(TR::WORDS % 4 == 0 && (kTileCap * 4) % 16 == 0, "16-byte aligned records");
-    static_assert(TR::WORDS >= kBoxRows, "the record space holds the flush's row table");
+    static_assert(TR::WORDS % 4 == 0 && (CAP * 4) % 16 == 0, "16-byte aligned records");
+    static_assert(TR::WORDS >= ROWS, "the record space holds the flush's row table");
 
     __shared__ float Rs[9];
     __shared__ float2 sh;
 
-    for (int e = lane; e < kTileCap; e += 32) {
+    for (int e = lane; e < CAP; e += 32) {
         if (DATA) acc[e] = make_float2(0.f, 0.f);
         if (WTS) wacc[e] = 0.f;
     }
@@ -1019,8 +1032,7 @@ __global__ void __launch_bounds__(kThreads) scatter_tile_kernel(
                 const int y1 = __reduce_max_sync(0xffffffffu, mine ? fy : -big) + FIRST + NT - 1;
                 const int z1 = __reduce_max_sync(0xffffffffu, mine ? fz : -big) + FIRST + NT - 1;
                 const int NX = x1 - x0 + 1, NY = y1 - y0 + 1, NZ = z1 - z0 + 1;
-                const bool boxed = NX <= kBoxPitch && NY <= kBoxRows && NZ <= kBoxRows &&
-                                   NY * NZ <= kBoxRows;
+                const bool boxed = NX <= PITCH && NY <= ROWS && NZ <= ROWS && NY * NZ <= ROWS;
                 // records of this pass's pixels
                 if (mine) {
                     float wx_[NT], wy_[NT], wz_[NT];
@@ -1050,7 +1062,7 @@ __global__ void __launch_bounds__(kThreads) scatter_tile_kernel(
                     // effective value: conj(g') on the mirrored pass (weights are real)
                     rf[TR::GX] = gp.x;
                     rf[TR::GY] = sg * gp.y;
-                    const int base = ((fz + FIRST - z0) * NY + (fy + FIRST - y0)) * kBoxPitch + (fx + FIRST - x0);
+                    const int base = ((fz + FIRST - z0) * NY + (fy + FIRST - y0)) * PITCH + (fx + FIRST - x0);
                     ri[TR::BASE] = (fx + FIRST <= 0 || !boxed) ? ~base : base;
                     ri[TR::FX] = fx;
                     ri[TR::FY] = fy;
@@ -1059,7 +1071,7 @@ __global__ void __launch_bounds__(kThreads) scatter_tile_kernel(
                 __syncwarp();
                 int toff[TPL];
 #pragma unroll
-                for (int m = 0; m < TPL; ++m) toff[m] = (ta[m] * NY + tb[m]) * kBoxPitch + tk;
+                for (int m = 0; m < TPL; ++m) toff[m] = (ta[m] * NY + tb[m]) * PITCH + tk;
                 // ---- scatter: one pixel at a time, lanes on its taps
                 for (unsigned pm = pmask; pm; pm &= pm - 1) {
                     const int j = __ffs(pm) - 1;
@@ -1156,7 +1168,7 @@ __global__ void __launch_bounds__(kThreads) scatter_tile_kernel(
                     for (int e = lane; e < nused; e += 32) {
                         const int r = (int)(((unsigned)e * mx) >> 16);
                         const int xi = e - r * NX;
-                        const int be = r * kBoxPitch + xi;
+                        const int be = r * PITCH + xi;
                         const int ux = x0 + xi;
                         bool hit = false;
                         float2 a = make_float2(0.f, 0.f);
@@ -1400,7 +1412,8 @@ template <int INTERP, bool DATA, bool WTS>
 void launch_scatter_tile(const Geom& g, const float2* P, const float* weights, const float* rot,
                          const float* shift, float2* VO, float* WO, int sms, cudaStream_t stream)
 {
-    const size_t per_warp = (DATA ? (size_t)kTileCap * 8 : 0) + (WTS ? (size_t)kTileCap * 4 : 0) +
+    constexpr size_t box_cap = BoxDims<INTERP>::CAP;
+    const size_t per_warp = (DATA ? box_cap * 8 : 0) + (WTS ? box_cap * 4 : 0) +
                             (size_t)TileRec<INTERP>::WORDS * 4;
     const size_t smem = per_warp * (kThreads / 32);
     auto kern = scatter_tile_kernel<INTERP, DATA, WTS>;
