@@ -883,36 +883,48 @@ __global__ void __launch_bounds__(BT) scatter_rows_kernel(
 // the x <= 0 planes take the exact per-tap rule, and tiles whose box would overflow (large
 // oversampling) use direct vector atomics.
 constexpr int kBoxPitch = 12;
-constexpr int kBoxRows = 81;                        // NY * NZ <= 9 * 9
 
-// Box of one warp, by interpolation.  Cubic: pitch 12, up to 81 rows (every 4 x 4 tile at
-// o = 1: floors span at most 3 sqrt(2) + 1 values, plus 3 taps, on each axis).  Linear: the
-// same tile spans at most 6 floors plus 1 tap, so 7 x 7 x 7: pitch 8 and 49 rows, a box of 392
-// voxels instead of 972, which leaves room for twice the resident warps.  Larger tiles (o > 1)
-// take the per-tap path.
+// Box of one warp, by interpolation.  Cubic: pitch 12 and 71 rows (every 4 x 4 tile at o = 1
+// spans at most 9 voxels per axis, so 81 rows would hold all of them; the 71 rows hold all but
+// about 3 in 10^4 tile passes and leave room for four CTAs per SM).  Linear: the same tile
+// spans at most 6 floors plus 1 tap, so 7 x 7 x 7: pitch 8 and 49 rows, a box of 392 voxels.
+// Larger tiles (o > 1) take the per-tap path.
 template <int INTERP>
 struct BoxDims {
     static constexpr int PITCH = INTERP == kCubic ? kBoxPitch : 8;
-    static constexpr int ROWS = INTERP == kCubic ? kBoxRows : 49;
+    static constexpr int ROWS = INTERP == kCubic ? 71 : 49;
     static constexpr int CAP = PITCH * ROWS;
 };
+
+// Threads of one scatter_tile_kernel CTA: as many warps as let the most CTAs fit in the SM's
+// 228 KB of shared memory (cubic 7 x 4 CTAs, cubic with weights 6 x 3, linear 8 x 4).
+template <int INTERP, bool WTS>
+__host__ __device__ constexpr int scatter_threads()
+{
+    return INTERP == kCubic ? (WTS ? 192 : 224) : 256;
+}
 constexpr int kTilePix = 16;                        // 4 x 4 pixels
 
 template <int INTERP>
 struct TileRec {
     static constexpr int NT = Taps<INTERP>::N;
     // One record per pixel, stored contiguously (array of structs): gx gy wt base (one
-    // 16-byte broadcast load) | wzy[NT*NT] | wx[NT] | fx fy fz.  base < 0 flags the per-tap
-    // path and holds ~base.
-    static constexpr int GX = 0, GY = 1, WT = 2, BASE = 3, WZY = 4, WX = 4 + NT * NT;
-    static constexpr int FX = WX + NT, FY = FX + 1, FZ = FX + 2;
+    // 16-byte broadcast load), then the weights, then fx fy fz.  base < 0 flags the per-tap
+    // path and holds ~base.  Linear: wzy[NT*NT] | wx[NT].  Cubic (SPLIT): wx[4] | wy[4] |
+    // wz in the order 0, 2, 1, 3, so that the z weights of a lane's two planes a and a + 2
+    // are one 8-byte load; the tap loop forms wz * wy (a 20-word record instead of 28).
+    static constexpr bool SPLIT = INTERP == kCubic;
+    static constexpr int GX = 0, GY = 1, WT = 2, BASE = 3, WZY = 4;
+    static constexpr int WX = SPLIT ? 4 : 4 + NT * NT;
+    static constexpr int WY = WX + NT, WZ = WY + NT;
+    static constexpr int FX = SPLIT ? WZ + NT : WX + NT, FY = FX + 1, FZ = FX + 2;
     static constexpr int USED = FZ + 1;
     static constexpr int STRIDE = (USED + 3) / 4 * 4;  // 16-byte aligned records
     static constexpr int WORDS = STRIDE * kTilePix;  // a multiple of 4: 16-byte aligned records
 };
 
 template <int INTERP, bool DATA, bool WTS>
-__global__ void __launch_bounds__(kThreads) scatter_tile_kernel(
+__global__ void __launch_bounds__(scatter_threads<INTERP, WTS>()) scatter_tile_kernel(
     const float2* __restrict__ proj, const float* __restrict__ wts,
     const float* __restrict__ rot, const float* __restrict__ shift,
     float2* __restrict__ vout, float* __restrict__ wout, Geom g, int splits, long long n_work)
@@ -924,7 +936,8 @@ __global__ void __launch_bounds__(kThreads) scatter_tile_kernel(
     constexpr int LPP = T < 32 ? T : 32;   // lanes per pixel
     constexpr int TPL = T / LPP;           // taps per lane
     static_assert(TPL == 1 || (NT == 4 && LPP == 32), "paired taps are z planes a and a + 2");
-    constexpr int NWARP = kThreads / 32;
+    static_assert(TR::SPLIT == (TPL == 2), "split weights go with paired taps");
+    constexpr int NWARP = scatter_threads<INTERP, WTS>() / 32;
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     extern __shared__ __align__(16) unsigned char sm_raw[];
     using BX = BoxDims<INTERP>;
@@ -1041,23 +1054,18 @@ __global__ void __launch_bounds__(kThreads) scatter_tile_kernel(
                     weights<INTERP>(ez - flz, wz_);
                     float* rf = recf + lane * TR::STRIDE;
                     int* ri = reci + lane * TR::STRIDE;
-                    if constexpr (TPL == 2) {
-                        // a lane's two taps are z planes a and a + 2 of one y row: store them
-                        // as an adjacent pair, read back with one 8-byte load
-#pragma unroll
-                        for (int a = 0; a < NT / 2; ++a)
-#pragma unroll
-                            for (int b = 0; b < NT; ++b)
-                                *reinterpret_cast<float2*>(rf + TR::WZY + 2 * (a * NT + b)) =
-                                    make_float2(wz_[a] * wy_[b], wz_[a + 2] * wy_[b]);
+                    if constexpr (TR::SPLIT) {
+                        *reinterpret_cast<float4*>(rf + TR::WX) = make_float4(wx_[0], wx_[1], wx_[2], wx_[3]);
+                        *reinterpret_cast<float4*>(rf + TR::WY) = make_float4(wy_[0], wy_[1], wy_[2], wy_[3]);
+                        *reinterpret_cast<float4*>(rf + TR::WZ) = make_float4(wz_[0], wz_[2], wz_[1], wz_[3]);
                     } else {
 #pragma unroll
                         for (int a = 0; a < NT; ++a)
 #pragma unroll
                             for (int b = 0; b < NT; ++b) rf[TR::WZY + a * NT + b] = wz_[a] * wy_[b];
-                    }
 #pragma unroll
-                    for (int k = 0; k < NT; ++k) rf[TR::WX + k] = wx_[k];
+                        for (int k = 0; k < NT; ++k) rf[TR::WX + k] = wx_[k];
+                    }
                     rf[TR::WT] = wt;
                     // effective value: conj(g') on the mirrored pass (weights are real)
                     rf[TR::GX] = gp.x;
@@ -1085,10 +1093,12 @@ __global__ void __launch_bounds__(kThreads) scatter_tile_kernel(
                         const int rb = __float_as_int(head.w);
                         const int base = rb < 0 ? ~rb : rb;
                         float wzy[TPL];
-                        if constexpr (TPL == 2) {
-                            const float2 pr = *reinterpret_cast<const float2*>(rf + TR::WZY + 2 * (ta[0] * NT + tb[0]));
-                            wzy[0] = pr.x;
-                            wzy[1] = pr.y;
+                        if constexpr (TR::SPLIT) {
+                            // z planes ta[0] and ta[0] + 2 of y row tb[0]
+                            const float2 zp = *reinterpret_cast<const float2*>(rf + TR::WZ + 2 * ta[0]);
+                            const float wyb = rf[TR::WY + tb[0]];
+                            wzy[0] = zp.x * wyb;
+                            wzy[1] = zp.y * wyb;
                         } else {
                             wzy[0] = rf[TR::WZY + ta[0] * NT + tb[0]];
                         }
@@ -1415,16 +1425,17 @@ void launch_scatter_tile(const Geom& g, const float2* P, const float* weights, c
     constexpr size_t box_cap = BoxDims<INTERP>::CAP;
     const size_t per_warp = (DATA ? box_cap * 8 : 0) + (WTS ? box_cap * 4 : 0) +
                             (size_t)TileRec<INTERP>::WORDS * 4;
-    const size_t smem = per_warp * (kThreads / 32);
+    constexpr int threads = scatter_threads<INTERP, WTS>(), nwarp = threads / 32;
+    const size_t smem = per_warp * nwarp;
     auto kern = scatter_tile_kernel<INTERP, DATA, WTS>;
     cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     const long long n_items = (long long)g.n_rec * g.n_pose;
     const long long ntiles = (long long)((g.Ho + 3) / 4) * ((g.Do + 3) / 4);
-    const int splits = (int)item_splits(n_items, 3LL * sms, (ntiles + kThreads / 32 - 1) / (kThreads / 32));
+    const int splits = (int)item_splits(n_items, 3LL * sms, (ntiles + nwarp - 1) / nwarp);
     const long long n_work = n_items * splits;
     const long long cap = 8LL * sms;
     const unsigned grid = (unsigned)(n_work < cap ? n_work : cap);
-    kern<<<grid, kThreads, smem, stream>>>(P, weights, rot, shift, VO, WO, g, splits, n_work);
+    kern<<<grid, threads, smem, stream>>>(P, weights, rot, shift, VO, WO, g, splits, n_work);
 }
 
 template <int NDIM, int INTERP>
