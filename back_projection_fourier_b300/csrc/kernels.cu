@@ -1208,6 +1208,209 @@ __global__ void __launch_bounds__(scatter_threads<INTERP, WTS>()) scatter_tile_k
     }
 }
 
+// Lane-per-pixel back-projection for linear 3D.  With 8 taps per pixel, the tile scatter's
+// lanes-on-taps mapping keeps only 8 lanes busy and pays its per-pixel record and loop costs 4
+// times over.  Here a warp takes an 8 x 4 tile of kept pixels, one pixel per lane, with the
+// pixel's weights in registers; every lane adds its 8 taps to the warp's private box of shared
+// memory with shared-memory float atomics (two pixels of the tile may share a voxel), and the
+// box is then added to the volume like the tile scatter's (row-offset table, one reduction per
+// non-zero voxel).  The box is dense, NX x NY x NZ voxels over the tile's footprint in the
+// effective frame (pixels with c_x < 0 in a second pass at c' = -c, conjugated; see
+// gather.cuh): at most 10 x 10 x 10 at o = 1, 264 voxels on average; tiles needing more than
+// kLaneCap voxels (about 2 in 10^4 at o = 1), wider than 16 voxels, or with taps on the x <= 0
+// planes take the exact per-tap rule with global atomics.
+constexpr int kLaneCap = 512;   // box voxels of one warp
+constexpr int kLaneRows = 96;   // box rows NY * NZ
+
+template <bool DATA, bool WTS>
+__host__ __device__ constexpr size_t lane_warp_bytes()
+{
+    return (DATA ? (size_t)kLaneCap * 8 : 0) + (WTS ? (size_t)kLaneCap * 4 : 0) + (size_t)kLaneRows * 4;
+}
+
+template <bool DATA, bool WTS>
+__global__ void __launch_bounds__(kThreads) scatter_lane_kernel(
+    const float2* __restrict__ proj, const float* __restrict__ wts,
+    const float* __restrict__ rot, const float* __restrict__ shift,
+    float2* __restrict__ vout, float* __restrict__ wout, Geom g, int splits, long long n_work)
+{
+    constexpr int NWARP = kThreads / 32;
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    extern __shared__ __align__(16) unsigned char sm_raw[];
+    unsigned char* mine = sm_raw + warp * lane_warp_bytes<DATA, WTS>();
+    float2* acc = reinterpret_cast<float2*>(mine);
+    float* wacc = reinterpret_cast<float*>(mine + (DATA ? kLaneCap * 8 : 0));
+    int* rowoff = reinterpret_cast<int*>(mine + (DATA ? kLaneCap * 8 : 0) + (WTS ? kLaneCap * 4 : 0));
+    __shared__ float Rs[9];
+    __shared__ float2 sh;
+
+    for (int e = lane; e < kLaneCap; e += 32) {
+        if (DATA) acc[e] = make_float2(0.f, 0.f);
+        if (WTS) wacc[e] = 0.f;
+    }
+    const int tiles_x = (g.Ho + 7) / 8, tiles_y = (g.Do + 3) / 4;
+    const int ntiles = tiles_x * tiles_y;
+    const int big = 1 << 28;
+
+    for (long long w = blockIdx.x; w < n_work; w += gridDim.x) {
+        const ItemRange ir = item_of(g, w, splits);
+        __syncthreads();
+        if (threadIdx.x < 9) {
+            const long long ri = (long long)(g.rot_shared ? 0 : ir.r) * g.n_pose + ir.p;
+            Rs[threadIdx.x] = g.o * __ldg(rot + ri * 9 + threadIdx.x);
+        }
+        if (threadIdx.x == 0) {
+            sh = make_float2(0.f, 0.f);
+            if (g.has_shift) {
+                const long long si = (long long)(g.sh_shared ? 0 : ir.r) * g.n_pose + ir.p;
+                sh = make_float2(__ldg(shift + si * 2), __ldg(shift + si * 2 + 1));
+            }
+        }
+        __syncthreads();
+        const float2* py = DATA ? proj + ir.item * g.img_elems : nullptr;
+        const float* pw = (WTS && wts) ? wts + ir.item * g.img_elems : nullptr;  // NULL: weight 1
+        float2* G = DATA ? vout + (long long)ir.r * g.rec_elems : nullptr;
+        float* Wt = WTS ? wout + (long long)ir.r * g.rec_elems : nullptr;
+
+        for (int tile = ir.part * NWARP + warp; tile < ntiles; tile += splits * NWARP) {
+            const int ti = tile / tiles_x, tj = tile - ti * tiles_x;
+            // lane l owns pixel (row 4 ti + l / 8, kx 8 tj + l % 8)
+            const int prow = 4 * ti + (lane >> 3), pkx = 8 * tj + (lane & 7);
+            bool kept = false;
+            int ky = 0;
+            float cx = 0.f, cy = 0.f, cz = 0.f;
+            if (prow < g.Do && pkx < g.Ho) {
+                ky = row_freq(prow, g.Do, g.halfo, g.centered);
+                kept = pkx * pkx + ky * ky <= g.rc2;
+                const float fkx = (float)pkx, fky = (float)ky;
+                cx = fmaf(Rs[0], fkx, Rs[1] * fky);
+                cy = fmaf(Rs[3], fkx, Rs[4] * fky);
+                cz = fmaf(Rs[6], fkx, Rs[7] * fky);
+            }
+            const unsigned kept_mask = __ballot_sync(0xffffffffu, kept);
+            if (!kept_mask) continue;
+            const unsigned neg_mask = __ballot_sync(0xffffffffu, kept && cx < 0.f);
+            float2 gp = make_float2(0.f, 0.f);
+            float wt = 1.f;
+            if (kept) {
+                if (DATA) {
+                    gp = __ldg(py + prow * g.Ho + pkx);
+                    if (g.has_shift)
+                        gp = cmul_conj(gp, shift_phase((float)pkx, (float)ky, sh.x, sh.y, g.Do_f, g.inv_Do));
+                }
+                if (WTS && pw) wt = __ldg(pw + prow * g.Ho + pkx);
+            }
+            for (int pass = 0; pass < 2; ++pass) {
+                const unsigned pmask = pass ? neg_mask : (kept_mask & ~neg_mask);
+                if (!pmask) continue;
+                const bool mine_px = (pmask >> lane) & 1u;
+                const float sg = pass ? -1.f : 1.f;
+                // effective coordinates, clamped like floor_frac (integer extents stay small)
+                const float lim = 8388608.0f;
+                const float ex = fminf(fmaxf(sg * cx, -lim), lim);
+                const float ey = fminf(fmaxf(sg * cy, -lim), lim);
+                const float ez = fminf(fmaxf(sg * cz, -lim), lim);
+                const float flx = floorf(ex), fly = floorf(ey), flz = floorf(ez);
+                const int fx = (int)flx, fy = (int)fly, fz = (int)flz;
+                // box of this pass's taps (floor and floor + 1 on each axis)
+                const int x0 = __reduce_min_sync(0xffffffffu, mine_px ? fx : big);
+                const int y0 = __reduce_min_sync(0xffffffffu, mine_px ? fy : big);
+                const int z0 = __reduce_min_sync(0xffffffffu, mine_px ? fz : big);
+                const int NX = __reduce_max_sync(0xffffffffu, mine_px ? fx : -big) + 2 - x0;
+                const int NY = __reduce_max_sync(0xffffffffu, mine_px ? fy : -big) + 2 - y0;
+                const int NZ = __reduce_max_sync(0xffffffffu, mine_px ? fz : -big) + 2 - z0;
+                const bool boxed = NX <= 16 && NY <= kLaneRows && NZ <= kLaneRows && NY * NZ <= kLaneRows &&
+                                   NX * NY * NZ <= kLaneCap;
+                if (mine_px) {
+                    const float frx = ex - flx, fry = ey - fly, frz = ez - flz;
+                    const float wxs[2] = {1.f - frx, frx}, wys[2] = {1.f - fry, fry}, wzs[2] = {1.f - frz, frz};
+                    // effective value: conj(g') on the mirrored pass (weights are real)
+                    const float vx = gp.x, vy = sg * gp.y;
+#pragma unroll
+                    for (int a = 0; a < 2; ++a)
+#pragma unroll
+                        for (int b = 0; b < 2; ++b) {
+                            const float wzy = wzs[a] * wys[b];
+#pragma unroll
+                            for (int k = 0; k < 2; ++k) {
+                                const float wgt = wzy * wxs[k];
+                                const int ux = fx + k;
+                                const bool direct = ux >= 1 || (ux == 0 && pass == 0);
+                                if (direct && boxed) {
+                                    const int e = ((fz + a - z0) * NY + (fy + b - y0)) * NX + (ux - x0);
+                                    if (DATA) {
+                                        atomicAdd(&acc[e].x, wgt * vx);
+                                        atomicAdd(&acc[e].y, wgt * vy);
+                                    }
+                                    if (WTS) atomicAdd(&wacc[e], wgt * wt);
+                                } else {
+                                    // target u (direct) or -u (mirrored, conjugate value)
+                                    int tx = ux, ty = fy + b, tz = fz + a;
+                                    float tim = vy;
+                                    if (!direct) {
+                                        tx = -tx;
+                                        ty = -ty;
+                                        tz = -tz;
+                                        tim = -tim;
+                                    }
+                                    const int iy = full_index(ty, g.Dv, g.halfv, g.centered);
+                                    const int iz = full_index(tz, g.Dv, g.halfv, g.centered);
+                                    if (tx >= 0 && tx <= g.halfv && iy >= 0 && iz >= 0) {
+                                        const long long off = ((long long)iz * g.Dv + iy) * g.Hv + tx;
+                                        if (DATA) atomicAdd(G + off, make_float2(wgt * vx, wgt * tim));
+                                        if (WTS) atomicAdd(Wt + off, wgt * wt);
+                                    }
+                                }
+                            }
+                        }
+                }
+                __syncwarp();
+                // ---- add the box to the volume (read and clear); rows r = zi * NY + yi, entries
+                // e = r * NX + xi (exact multiply-shift: e < 512 with NX <= 16, r < 96 with
+                // NY <= 96); only non-zero entries are added and cleared
+                if (boxed) {
+                    const int nrows = NY * NZ;
+                    const unsigned my = (65536u + NY - 1) / NY;
+                    for (int r = lane; r < nrows; r += 32) {
+                        const int zi = (int)(((unsigned)r * my) >> 16);
+                        const int iy = full_index(y0 + r - zi * NY, g.Dv, g.halfv, g.centered);
+                        const int iz = full_index(z0 + zi, g.Dv, g.halfv, g.centered);
+                        rowoff[r] = (iy >= 0 && iz >= 0) ? (iz * g.Dv + iy) * g.Hv : -1;
+                    }
+                    __syncwarp();
+                    const unsigned mx = (65536u + NX - 1) / NX;
+                    const int nused = nrows * NX;
+                    for (int e = lane; e < nused; e += 32) {
+                        const int r = (int)(((unsigned)e * mx) >> 16);
+                        const int ux = x0 + (e - r * NX);
+                        bool hit = false;
+                        float2 c = make_float2(0.f, 0.f);
+                        float b = 0.f;
+                        if (DATA) {
+                            c = acc[e];
+                            hit = c.x != 0.f || c.y != 0.f;
+                        }
+                        if (WTS) {
+                            b = wacc[e];
+                            hit = hit || b != 0.f;
+                        }
+                        if (hit) {
+                            const int ro = rowoff[r];
+                            if (ro >= 0 && ux >= 0 && ux <= g.halfv) {
+                                if (DATA && (c.x != 0.f || c.y != 0.f)) atomicAdd(G + ro + ux, c);
+                                if (WTS && b != 0.f) atomicAdd(Wt + ro + ux, b);
+                            }
+                            if (DATA) acc[e] = make_float2(0.f, 0.f);
+                            if (WTS) wacc[e] = 0.f;
+                        }
+                    }
+                }
+                __syncwarp();
+            }
+        }
+    }
+}
+
 // Weight-volume part of the back-projection's backward: per kept pixel the real
 // interpolation v of the upstream weight-volume gradient (that is dL/d weight) and, for the
 // rotation gradient, weight * o q_b dv/dc_a summed per item (exact per-tap path).
@@ -1438,6 +1641,22 @@ void launch_scatter_tile(const Geom& g, const float2* P, const float* weights, c
     kern<<<grid, threads, smem, stream>>>(P, weights, rot, shift, VO, WO, g, splits, n_work);
 }
 
+template <bool DATA, bool WTS>
+void launch_scatter_lane(const Geom& g, const float2* P, const float* weights, const float* rot,
+                         const float* shift, float2* VO, float* WO, int sms, cudaStream_t stream)
+{
+    const size_t smem = lane_warp_bytes<DATA, WTS>() * (kThreads / 32);
+    auto kern = scatter_lane_kernel<DATA, WTS>;
+    cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    const long long n_items = (long long)g.n_rec * g.n_pose;
+    const long long ntiles = (long long)((g.Ho + 7) / 8) * ((g.Do + 3) / 4);
+    const int splits = (int)item_splits(n_items, 3LL * sms, (ntiles + kThreads / 32 - 1) / (kThreads / 32));
+    const long long n_work = n_items * splits;
+    const long long cap = 8LL * sms;
+    const unsigned grid = (unsigned)(n_work < cap ? n_work : cap);
+    kern<<<grid, kThreads, smem, stream>>>(P, weights, rot, shift, VO, WO, g, splits, n_work);
+}
+
 template <int NDIM, int INTERP>
 void launch_backproject_t(const Geom& g, const float2* P, const float* weights, const float* rot,
                           const float* shift, float2* VO, float* WO, int sms, cudaStream_t stream)
@@ -1448,7 +1667,14 @@ void launch_backproject_t(const Geom& g, const float2* P, const float* weights, 
                                                                            WO, g, s.splits, s.n_work);
         return;
     }
-    if constexpr (NDIM == 3) {
+    if constexpr (NDIM == 3 && INTERP == kLinear) {
+        if (VO && WO)
+            launch_scatter_lane<true, true>(g, P, weights, rot, shift, VO, WO, sms, stream);
+        else if (VO)
+            launch_scatter_lane<true, false>(g, P, weights, rot, shift, VO, WO, sms, stream);
+        else
+            launch_scatter_lane<false, true>(g, P, weights, rot, shift, VO, WO, sms, stream);
+    } else if constexpr (NDIM == 3) {
         if (VO && WO)
             launch_scatter_tile<INTERP, true, true>(g, P, weights, rot, shift, VO, WO, sms, stream);
         else if (VO)
