@@ -884,24 +884,25 @@ __global__ void __launch_bounds__(BT) scatter_rows_kernel(
 // oversampling) use direct vector atomics.
 constexpr int kBoxPitch = 12;
 
-// Box of one warp, by interpolation.  Cubic: pitch 12 and 71 rows (every 4 x 4 tile at o = 1
-// spans at most 9 voxels per axis, so 81 rows would hold all of them; the 71 rows hold all but
-// about 3 in 10^4 tile passes and leave room for four CTAs per SM).  Linear: the same tile
-// spans at most 6 floors plus 1 tap, so 7 x 7 x 7: pitch 8 and 49 rows, a box of 392 voxels.
-// Larger tiles (o > 1) take the per-tap path.
-template <int INTERP>
+// Box of one warp, by interpolation.  Cubic: pitch 12 (every 4 x 4 tile at o = 1 spans at
+// most 9 voxels per axis, so 81 rows would hold all of them); 71 rows hold all but about 3 in
+// 10^4 tile passes and fit four CTAs of 7 warps per SM; with the weight box, 63 rows (all but
+// about 1 %) fit three CTAs of 7 warps instead of 6, which gains more than the extra per-tap
+// passes cost.  Linear: the same tile spans at most 6 floors plus 1 tap, so 7 x 7 x 7: pitch 8
+// and 49 rows, a box of 392 voxels.  Larger tiles (o > 1) take the per-tap path.
+template <int INTERP, bool WTS>
 struct BoxDims {
     static constexpr int PITCH = INTERP == kCubic ? kBoxPitch : 8;
-    static constexpr int ROWS = INTERP == kCubic ? 71 : 49;
+    static constexpr int ROWS = INTERP == kCubic ? (WTS ? 63 : 71) : 49;
     static constexpr int CAP = PITCH * ROWS;
 };
 
 // Threads of one scatter_tile_kernel CTA: as many warps as let the most CTAs fit in the SM's
-// 228 KB of shared memory (cubic 7 x 4 CTAs, cubic with weights 6 x 3, linear 8 x 4).
+// 228 KB of shared memory (cubic 7 x 4 CTAs, cubic with weights 7 x 3, linear 8 x 4).
 template <int INTERP, bool WTS>
 __host__ __device__ constexpr int scatter_threads()
 {
-    return INTERP == kCubic ? (WTS ? 192 : 224) : 256;
+    return INTERP == kCubic ? 224 : 256;
 }
 constexpr int kTilePix = 16;                        // 4 x 4 pixels
 
@@ -940,7 +941,7 @@ __global__ void __launch_bounds__(scatter_threads<INTERP, WTS>()) scatter_tile_k
     constexpr int NWARP = scatter_threads<INTERP, WTS>() / 32;
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     extern __shared__ __align__(16) unsigned char sm_raw[];
-    using BX = BoxDims<INTERP>;
+    using BX = BoxDims<INTERP, WTS>;
     constexpr int CAP = BX::CAP, PITCH = BX::PITCH, ROWS = BX::ROWS;
     // per warp: acc[CAP] float2 | wacc[CAP] float | records (TR::WORDS words)
     float2* acc = reinterpret_cast<float2*>(sm_raw) + warp * (DATA ? CAP : 0);
@@ -1625,7 +1626,7 @@ template <int INTERP, bool DATA, bool WTS>
 void launch_scatter_tile(const Geom& g, const float2* P, const float* weights, const float* rot,
                          const float* shift, float2* VO, float* WO, int sms, cudaStream_t stream)
 {
-    constexpr size_t box_cap = BoxDims<INTERP>::CAP;
+    constexpr size_t box_cap = BoxDims<INTERP, WTS>::CAP;
     const size_t per_warp = (DATA ? box_cap * 8 : 0) + (WTS ? box_cap * 4 : 0) +
                             (size_t)TileRec<INTERP>::WORDS * 4;
     constexpr int threads = scatter_threads<INTERP, WTS>(), nwarp = threads / 32;
