@@ -24,6 +24,9 @@ CASES = [
     (3, 1, 1, 1.0, 2, 2, -1.0, True, 1, 1, 5),
     (3, 1, 0, 1.0, 30, 30, -1.0, True, 2, 2, 7),
     (3, 0, 1, 1.25, 40, 32, 12.0, True, 3, 1, 6),
+    # linear at o = 2: many 8 x 4 tiles of the linear scatter exceed its box (wider than 16
+    # voxels) and take the per-tap path with global atomics
+    (3, 0, 1, 2.0, 48, 24, -1.0, True, 2, 1, 5),
     (2, 1, 1, 1.0, 48, 48, -1.0, True, 5, 5, 3),
     (2, 0, 0, 1.0, 30, 30, -1.0, True, 3, 1, 4),
     (2, 1, 0, 1.5, 36, 24, 10.0, False, 4, 4, 2),
