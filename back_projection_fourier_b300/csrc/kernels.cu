@@ -885,15 +885,16 @@ __global__ void __launch_bounds__(BT) scatter_rows_kernel(
 constexpr int kBoxPitch = 12;
 
 // Box of one warp, by interpolation.  Cubic: pitch 12 (every 4 x 4 tile at o = 1 spans at
-// most 9 voxels per axis, so 81 rows would hold all of them); 71 rows hold all but about 3 in
-// 10^4 tile passes and fit four CTAs of 7 warps per SM; with the weight box, 63 rows (all but
-// about 1 %) fit three CTAs of 7 warps instead of 6, which gains more than the extra per-tap
-// passes cost.  Linear: the same tile spans at most 6 floors plus 1 tap, so 7 x 7 x 7: pitch 8
-// and 49 rows, a box of 392 voxels.  Larger tiles (o > 1) take the per-tap path.
+// most 9 voxels per axis, so 81 rows would hold all of them).  72 rows hold all but about 1 in
+// 10^4 tile passes (NY * NZ = 8 x 9 is common, more is rare) and, with no static shared memory,
+// fit exactly four CTAs of 7 warps per SM; with the weight box, 64 rows (all but 0.6 %: the
+// common 8 x 9 boxes take the per-tap path) fit three CTAs of 7 warps instead of 6.  Linear:
+// the same tile spans at most 6 floors plus 1 tap, so 7 x 7 x 7: pitch 8 and 49 rows, a box of
+// 392 voxels.  Larger tiles (o > 1) take the per-tap path.
 template <int INTERP, bool WTS>
 struct BoxDims {
     static constexpr int PITCH = INTERP == kCubic ? kBoxPitch : 8;
-    static constexpr int ROWS = INTERP == kCubic ? (WTS ? 63 : 71) : 49;
+    static constexpr int ROWS = INTERP == kCubic ? (WTS ? 64 : 72) : 49;
     static constexpr int CAP = PITCH * ROWS;
 };
 
@@ -953,9 +954,6 @@ __global__ void __launch_bounds__(scatter_threads<INTERP, WTS>()) scatter_tile_k
     static_assert(TR::WORDS % 4 == 0 && (CAP * 4) % 16 == 0, "16-byte aligned records");
     static_assert(TR::WORDS >= ROWS, "the record space holds the flush's row table");
 
-    __shared__ float Rs[9];
-    __shared__ float2 sh;
-
     for (int e = lane; e < CAP; e += 32) {
         if (DATA) acc[e] = make_float2(0.f, 0.f);
         if (WTS) wacc[e] = 0.f;
@@ -973,22 +971,22 @@ __global__ void __launch_bounds__(scatter_threads<INTERP, WTS>()) scatter_tile_k
     const int tiles_x = (g.Ho + 3) / 4, tiles_y = (g.Do + 3) / 4;
     const int ntiles = tiles_x * tiles_y;
 
-    // work unit = (item, part): part takes every splits-th round of NWARP tiles
+    // work unit = (item, part): part takes every splits-th round of NWARP tiles.  Every thread
+    // reads the item's rotation (scaled by o) and shift into registers itself: the kernel needs
+    // no static shared memory (its whole budget goes to the boxes) and no barrier between items.
     for (long long w = blockIdx.x; w < n_work; w += gridDim.x) {
         const ItemRange ir = item_of(g, w, splits);
-        __syncthreads();
-        if (threadIdx.x < 9) {
+        float Rs[9];
+        {
             const long long ri = (long long)(g.rot_shared ? 0 : ir.r) * g.n_pose + ir.p;
-            Rs[threadIdx.x] = g.o * __ldg(rot + ri * 9 + threadIdx.x);
+#pragma unroll
+            for (int k = 0; k < 9; ++k) Rs[k] = g.o * __ldg(rot + ri * 9 + k);
         }
-        if (threadIdx.x == 0) {
-            sh = make_float2(0.f, 0.f);
-            if (g.has_shift) {
-                const long long si = (long long)(g.sh_shared ? 0 : ir.r) * g.n_pose + ir.p;
-                sh = make_float2(__ldg(shift + si * 2), __ldg(shift + si * 2 + 1));
-            }
+        float2 sh = make_float2(0.f, 0.f);
+        if (g.has_shift) {
+            const long long si = (long long)(g.sh_shared ? 0 : ir.r) * g.n_pose + ir.p;
+            sh = make_float2(__ldg(shift + si * 2), __ldg(shift + si * 2 + 1));
         }
-        __syncthreads();
         const float2* py = DATA ? proj + ir.item * g.img_elems : nullptr;
         const float* pw = (WTS && wts) ? wts + ir.item * g.img_elems : nullptr;  // NULL: weight 1
         float2* G = DATA ? vout + (long long)ir.r * g.rec_elems : nullptr;
