@@ -869,11 +869,11 @@ __global__ void __launch_bounds__(BT) scatter_rows_kernel(
     }
 }
 
-// Warp-tile back-projection for 3D.  A warp takes a 4 x 4 tile of kept pixels of one item
-// and accumulates the tile's taps in a private box of shared memory that covers the tile's
-// footprint (the axis-aligned box of its taps in the effective frame, at most 9^3 voxels
-// for o = 1).  The warp walks the tile's pixels one at a time with its lanes on the
-// pixel's taps (64 for cubic: two per lane); one pixel's taps are distinct voxels, so the
+// Warp-tile back-projection for cubic 3D.  A warp takes a 4 x 4 tile of kept pixels of one
+// item and accumulates the tile's taps in a private box of shared memory that covers the
+// tile's footprint (the axis-aligned box of its taps in the effective frame, at most 9^3
+// voxels for o = 1).  The warp walks the tile's pixels one at a time with its lanes on the
+// pixel's 64 taps (two per lane); one pixel's taps are distinct voxels, so the
 // lanes read-modify-write shared memory without atomics and __syncwarp orders successive
 // pixels.  The box rows have a pitch of 12 voxels: a half-warp's 16 taps (4 y rows x 4 x
 // taps, 8-byte values) then fall in 16 distinct bank pairs.  The finished box is added to
@@ -884,65 +884,50 @@ __global__ void __launch_bounds__(BT) scatter_rows_kernel(
 // oversampling) use direct vector atomics.
 constexpr int kBoxPitch = 12;
 
-// Box of one warp, by interpolation.  Cubic: pitch 12 (every 4 x 4 tile at o = 1 spans at
-// most 9 voxels per axis, so 81 rows would hold all of them).  72 rows hold all but about 1 in
-// 10^4 tile passes (NY * NZ = 8 x 9 is common, more is rare) and, with no static shared memory,
-// fit exactly four CTAs of 7 warps per SM; with the weight box, 64 rows (all but 0.6 %: the
-// common 8 x 9 boxes take the per-tap path) fit three CTAs of 7 warps instead of 6.  Linear:
-// the same tile spans at most 6 floors plus 1 tap, so 7 x 7 x 7: pitch 8 and 49 rows, a box of
-// 392 voxels.  Larger tiles (o > 1) take the per-tap path.
-template <int INTERP, bool WTS>
+// Box of one warp (cubic; the linear 3D scatter is scatter_lane_kernel).  Pitch 12: every
+// 4 x 4 tile at o = 1 spans at most 9 voxels per axis, so 81 rows would hold all of them.
+// 72 rows hold all but about 1 in 10^4 tile passes (NY * NZ = 8 x 9 is common, more is rare)
+// and, with no static shared memory, fit exactly four CTAs of 7 warps per SM; with the weight
+// box, 64 rows (all but 0.6 %: the common 8 x 9 boxes take the per-tap path) fit three CTAs of
+// 7 warps instead of 6.  Larger tiles (o > 1) take the per-tap path.
+template <bool WTS>
 struct BoxDims {
-    static constexpr int PITCH = INTERP == kCubic ? kBoxPitch : 8;
-    static constexpr int ROWS = INTERP == kCubic ? (WTS ? 64 : 72) : 49;
+    static constexpr int PITCH = kBoxPitch;
+    static constexpr int ROWS = WTS ? 64 : 72;
     static constexpr int CAP = PITCH * ROWS;
 };
 
-// Threads of one scatter_tile_kernel CTA: as many warps as let the most CTAs fit in the SM's
-// 228 KB of shared memory (cubic 7 x 4 CTAs, cubic with weights 7 x 3, linear 8 x 4).
-template <int INTERP, bool WTS>
-__host__ __device__ constexpr int scatter_threads()
-{
-    return INTERP == kCubic ? 224 : 256;
-}
+// Threads of one scatter_tile_kernel CTA: 7 warps, so that four CTAs (three with the weight
+// box) fit in the SM's 228 KB of shared memory.
+constexpr int kTileThreads = 224;
 constexpr int kTilePix = 16;                        // 4 x 4 pixels
 
-template <int INTERP>
+// One record per pixel, stored contiguously (array of structs): gx gy wt base (one 16-byte
+// broadcast load) | wx[4] | wy[4] | wz in the order 0, 2, 1, 3, so that the z weights of a
+// lane's two planes a and a + 2 are one 8-byte load (the tap loop forms wz * wy) | fx fy fz.
+// base < 0 flags the per-tap path and holds ~base.
 struct TileRec {
-    static constexpr int NT = Taps<INTERP>::N;
-    // One record per pixel, stored contiguously (array of structs): gx gy wt base (one
-    // 16-byte broadcast load), then the weights, then fx fy fz.  base < 0 flags the per-tap
-    // path and holds ~base.  Linear: wzy[NT*NT] | wx[NT].  Cubic (SPLIT): wx[4] | wy[4] |
-    // wz in the order 0, 2, 1, 3, so that the z weights of a lane's two planes a and a + 2
-    // are one 8-byte load; the tap loop forms wz * wy (a 20-word record instead of 28).
-    static constexpr bool SPLIT = INTERP == kCubic;
-    static constexpr int GX = 0, GY = 1, WT = 2, BASE = 3, WZY = 4;
-    static constexpr int WX = SPLIT ? 4 : 4 + NT * NT;
-    static constexpr int WY = WX + NT, WZ = WY + NT;
-    static constexpr int FX = SPLIT ? WZ + NT : WX + NT, FY = FX + 1, FZ = FX + 2;
-    static constexpr int USED = FZ + 1;
-    static constexpr int STRIDE = (USED + 3) / 4 * 4;  // 16-byte aligned records
+    static constexpr int GX = 0, GY = 1, WT = 2, BASE = 3, WX = 4, WY = 8, WZ = 12;
+    static constexpr int FX = 16, FY = 17, FZ = 18;
+    static constexpr int STRIDE = 20;                // 16-byte aligned records
     static constexpr int WORDS = STRIDE * kTilePix;  // a multiple of 4: 16-byte aligned records
 };
 
 template <int INTERP, bool DATA, bool WTS>
-__global__ void __launch_bounds__(scatter_threads<INTERP, WTS>()) scatter_tile_kernel(
+__global__ void __launch_bounds__(kTileThreads) scatter_tile_kernel(
     const float2* __restrict__ proj, const float* __restrict__ wts,
     const float* __restrict__ rot, const float* __restrict__ shift,
     float2* __restrict__ vout, float* __restrict__ wout, Geom g, int splits, long long n_work)
 {
-    using TR = TileRec<INTERP>;
+    static_assert(INTERP == kCubic, "the linear 3D scatter is scatter_lane_kernel");
+    using TR = TileRec;
     constexpr int NT = Taps<INTERP>::N;
     constexpr int FIRST = Taps<INTERP>::first;
-    constexpr int T = NT * NT * NT;        // taps per pixel
-    constexpr int LPP = T < 32 ? T : 32;   // lanes per pixel
-    constexpr int TPL = T / LPP;           // taps per lane
-    static_assert(TPL == 1 || (NT == 4 && LPP == 32), "paired taps are z planes a and a + 2");
-    static_assert(TR::SPLIT == (TPL == 2), "split weights go with paired taps");
-    constexpr int NWARP = scatter_threads<INTERP, WTS>() / 32;
+    constexpr int TPL = 2;                 // taps per lane: 64 taps on 32 lanes
+    constexpr int NWARP = kTileThreads / 32;
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     extern __shared__ __align__(16) unsigned char sm_raw[];
-    using BX = BoxDims<INTERP, WTS>;
+    using BX = BoxDims<WTS>;
     constexpr int CAP = BX::CAP, PITCH = BX::PITCH, ROWS = BX::ROWS;
     // per warp: acc[CAP] float2 | wacc[CAP] float | records (TR::WORDS words)
     float2* acc = reinterpret_cast<float2*>(sm_raw) + warp * (DATA ? CAP : 0);
@@ -967,7 +952,6 @@ __global__ void __launch_bounds__(scatter_threads<INTERP, WTS>()) scatter_tile_k
         ta[m] = q / (NT * NT);
         tb[m] = (q / NT) % NT;
     }
-    const bool tap_lane = lane < LPP;
     const int tiles_x = (g.Ho + 3) / 4, tiles_y = (g.Do + 3) / 4;
     const int ntiles = tiles_x * tiles_y;
 
@@ -1053,18 +1037,9 @@ __global__ void __launch_bounds__(scatter_threads<INTERP, WTS>()) scatter_tile_k
                     weights<INTERP>(ez - flz, wz_);
                     float* rf = recf + lane * TR::STRIDE;
                     int* ri = reci + lane * TR::STRIDE;
-                    if constexpr (TR::SPLIT) {
-                        *reinterpret_cast<float4*>(rf + TR::WX) = make_float4(wx_[0], wx_[1], wx_[2], wx_[3]);
-                        *reinterpret_cast<float4*>(rf + TR::WY) = make_float4(wy_[0], wy_[1], wy_[2], wy_[3]);
-                        *reinterpret_cast<float4*>(rf + TR::WZ) = make_float4(wz_[0], wz_[2], wz_[1], wz_[3]);
-                    } else {
-#pragma unroll
-                        for (int a = 0; a < NT; ++a)
-#pragma unroll
-                            for (int b = 0; b < NT; ++b) rf[TR::WZY + a * NT + b] = wz_[a] * wy_[b];
-#pragma unroll
-                        for (int k = 0; k < NT; ++k) rf[TR::WX + k] = wx_[k];
-                    }
+                    *reinterpret_cast<float4*>(rf + TR::WX) = make_float4(wx_[0], wx_[1], wx_[2], wx_[3]);
+                    *reinterpret_cast<float4*>(rf + TR::WY) = make_float4(wy_[0], wy_[1], wy_[2], wy_[3]);
+                    *reinterpret_cast<float4*>(rf + TR::WZ) = make_float4(wz_[0], wz_[2], wz_[1], wz_[3]);
                     rf[TR::WT] = wt;
                     // effective value: conj(g') on the mirrored pass (weights are real)
                     rf[TR::GX] = gp.x;
@@ -1082,7 +1057,7 @@ __global__ void __launch_bounds__(scatter_threads<INTERP, WTS>()) scatter_tile_k
                 // ---- scatter: one pixel at a time, lanes on its taps
                 for (unsigned pm = pmask; pm; pm &= pm - 1) {
                     const int j = __ffs(pm) - 1;
-                    if (tap_lane) {
+                    {
                         const float* rf = recf + j * TR::STRIDE;
                         const int* ri = reci + j * TR::STRIDE;
                         const float4 head = *reinterpret_cast<const float4*>(rf);
@@ -1091,16 +1066,10 @@ __global__ void __launch_bounds__(scatter_threads<INTERP, WTS>()) scatter_tile_k
                         const float wxk = rf[TR::WX + tk];
                         const int rb = __float_as_int(head.w);
                         const int base = rb < 0 ? ~rb : rb;
-                        float wzy[TPL];
-                        if constexpr (TR::SPLIT) {
-                            // z planes ta[0] and ta[0] + 2 of y row tb[0]
-                            const float2 zp = *reinterpret_cast<const float2*>(rf + TR::WZ + 2 * ta[0]);
-                            const float wyb = rf[TR::WY + tb[0]];
-                            wzy[0] = zp.x * wyb;
-                            wzy[1] = zp.y * wyb;
-                        } else {
-                            wzy[0] = rf[TR::WZY + ta[0] * NT + tb[0]];
-                        }
+                        // z planes ta[0] and ta[0] + 2 of y row tb[0]
+                        const float2 zp = *reinterpret_cast<const float2*>(rf + TR::WZ + 2 * ta[0]);
+                        const float wyb = rf[TR::WY + tb[0]];
+                        const float wzy[TPL] = {zp.x * wyb, zp.y * wyb};
                         if (rb >= 0) {
 #pragma unroll
                             for (int m = 0; m < TPL; ++m) {
@@ -1624,10 +1593,10 @@ template <int INTERP, bool DATA, bool WTS>
 void launch_scatter_tile(const Geom& g, const float2* P, const float* weights, const float* rot,
                          const float* shift, float2* VO, float* WO, int sms, cudaStream_t stream)
 {
-    constexpr size_t box_cap = BoxDims<INTERP, WTS>::CAP;
+    constexpr size_t box_cap = BoxDims<WTS>::CAP;
     const size_t per_warp = (DATA ? box_cap * 8 : 0) + (WTS ? box_cap * 4 : 0) +
-                            (size_t)TileRec<INTERP>::WORDS * 4;
-    constexpr int threads = scatter_threads<INTERP, WTS>(), nwarp = threads / 32;
+                            (size_t)TileRec::WORDS * 4;
+    constexpr int threads = kTileThreads, nwarp = threads / 32;
     const size_t smem = per_warp * nwarp;
     auto kern = scatter_tile_kernel<INTERP, DATA, WTS>;
     cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
