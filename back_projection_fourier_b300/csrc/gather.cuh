@@ -16,8 +16,10 @@
 // multiple of the window for WIN = 2, and of 4 elements when Dv % 4 == 0, which the host
 // requires for WIN = 4), so the shifted x weights are formed once per y tap.
 //   WIN = kGrouped: rows read from the grouped copy of the volume (see expand_groups in
-//   kernels.cu), where element NT*i + k holds tap i + k: one aligned 32-byte (cubic) or
-//   16-byte (linear) load per row, always within one sector.
+//   kernels.cu), where group i of a row holds the NT taps i .. i + NT - 1: one aligned
+//   32-byte (cubic) or 16-byte (linear) load per row, always within one sector.  Its rows
+//   also hold the groups starting at x = -(NT - 1) .. -1, whose taps left of x = 0 are the
+//   conjugate mirror values, so pixels near the x = 0 plane read it in the original frame.
 #pragma once
 
 #include "tp_device.cuh"
@@ -45,46 +47,68 @@ template <int NDIM, int INTERP, bool DERIV>
 struct FastTaps {
     static constexpr int NT = Taps<INTERP>::N;
     static constexpr int NZ = NDIM == 3 ? NT : 1;
-    int x0;            // first x tap (>= 1)
-    int zoff[NZ];      // iz * Dv * Hv (0 for 2D)
-    int yrow[NT];      // iy * Hv
+    int x0;            // first x tap (>= 1; >= -(NT - 1) on the grouped copy)
+    int zoff[NZ];      // iz * Dv * row length (0 for 2D)
+    int yrow[NT];      // iy * row length
     float wx[NT], wy[NT], wz[NZ];
     float dx[DERIV ? NT : 1], dy[DERIV ? NT : 1], dz[DERIV ? NZ : 1];
 };
 
 // Set up the effective-frame taps of a pixel.  Returns false when the pixel needs the
-// general per-tap path.  `flip` is set when the sample is conjugated (c_x < 0).
-template <int NDIM, int INTERP, bool DERIV>
+// general per-tap path.  `flip` is set when the sample is conjugated.
+//   EXT = false (volume read in place): every pixel with c_x < 0 is flipped, and the pixel is
+//   fast when its taps lie in 1 <= x <= Dv/2.
+//   EXT = true (grouped copy, whose rows also hold the mirrored taps x = -(NT-1) .. -1):
+//   only pixels with o c_x <= -NT/2 are flipped, which puts their first tap at x >= 1, and
+//   the rest are read in the original frame, first tap x >= -(NT - 1).  A tap left of x = 0
+//   then reads the mirrored row (-y, -z); when a direct y or z tap of such a pixel lies
+//   outside the stored band its mirror may not, and the pixel takes the general path.
+template <int NDIM, int INTERP, bool DERIV, bool EXT>
 __device__ __forceinline__ bool fast_taps(const Geom& g, const float* R, float kx, float ky,
                                           FastTaps<NDIM, INTERP, DERIV>& t, bool& flip)
 {
     constexpr int NT = Taps<INTERP>::N;
     constexpr int K = NDIM;
+    const int hv = EXT ? g.grow : g.Hv;  // row pitch in elements (groups)
     dfloat cx = dot2(R[0], kx, R[1], ky);
     dfloat cy = dot2(R[K], kx, R[K + 1], ky);
-    flip = cx.hi < 0.f || (cx.hi == 0.f && cx.lo < 0.f);
-    if (flip) {
-        cx = {-cx.hi, -cx.lo};
-        cy = {-cy.hi, -cy.lo};
-    }
     int b;
     float f;
-    floor_frac(cx, g.o, g.o_is_one, b, f);
+    if constexpr (EXT) {
+        // decided on o c_x: negation commutes exactly with the scaling by o
+        cx = scale_coord(cx, g.o, g.o_is_one);
+        constexpr float T = -0.5f * NT;
+        flip = cx.hi < T || (cx.hi == T && cx.lo <= 0.f);
+        if (flip) {
+            cx = {-cx.hi, -cx.lo};
+            cy = {-cy.hi, -cy.lo};
+        }
+        floor_split(cx, b, f);
+    } else {
+        flip = cx.hi < 0.f || (cx.hi == 0.f && cx.lo < 0.f);
+        if (flip) {
+            cx = {-cx.hi, -cx.lo};
+            cy = {-cy.hi, -cy.lo};
+        }
+        floor_frac(cx, g.o, g.o_is_one, b, f);
+    }
     t.x0 = b + Taps<INTERP>::first;
-    if (t.x0 < 1 || t.x0 + NT - 1 > g.halfv) return false;
+    if (t.x0 < (EXT ? 1 - NT : 1) || t.x0 + NT - 1 > g.halfv) return false;
     weights<INTERP>(f, t.wx);
     if constexpr (DERIV) dweights<INTERP>(f, t.dx);
     floor_frac(cy, g.o, g.o_is_one, b, f);
     weights<INTERP>(f, t.wy);
     if constexpr (DERIV) dweights<INTERP>(f, t.dy);
+    bool outside = false;  // a direct y or z tap outside the stored band
 #pragma unroll
     for (int k = 0; k < NT; ++k) {
         const int iy = full_index(b + Taps<INTERP>::first + k, g.Dv, g.halfv, g.centered);
         if (iy < 0) {
             t.wy[k] = 0.f;
             if constexpr (DERIV) t.dy[k] = 0.f;
+            outside = true;
         }
-        t.yrow[k] = (iy < 0 ? 0 : iy) * g.Hv;
+        t.yrow[k] = (iy < 0 ? 0 : iy) * hv;
     }
     if constexpr (NDIM == 3) {
         dfloat cz = dot2(R[6], kx, R[7], ky);
@@ -92,13 +116,14 @@ __device__ __forceinline__ bool fast_taps(const Geom& g, const float* R, float k
         floor_frac(cz, g.o, g.o_is_one, b, f);
         weights<INTERP>(f, t.wz);
         if constexpr (DERIV) dweights<INTERP>(f, t.dz);
-        const int plane = g.Dv * g.Hv;
+        const int plane = EXT ? g.gplane : g.Dv * g.Hv;
 #pragma unroll
         for (int k = 0; k < NT; ++k) {
             const int iz = full_index(b + Taps<INTERP>::first + k, g.Dv, g.halfv, g.centered);
             if (iz < 0) {
                 t.wz[k] = 0.f;
                 if constexpr (DERIV) t.dz[k] = 0.f;
+                outside = true;
             }
             t.zoff[k] = (iz < 0 ? 0 : iz) * plane;
         }
@@ -107,7 +132,7 @@ __device__ __forceinline__ bool fast_taps(const Geom& g, const float* R, float k
         t.wz[0] = 1.f;
         if constexpr (DERIV) t.dz[0] = 0.f;
     }
-    return true;
+    return !(EXT && outside && t.x0 < 0);
 }
 
 // Row sums over the x taps of one row: rs = sum_k wx[k] V[row + x0 + k] and, with DERIV,
@@ -292,7 +317,8 @@ __device__ __forceinline__ void gather_fast(const float2* __restrict__ V,
     v = make_float2(0.f, 0.f);
     if constexpr (DERIV) dv[0] = dv[1] = dv[2] = make_float2(0.f, 0.f);
     constexpr int M = WIN == kGrouped ? NT : 1;  // elements per voxel of V
-    const float2* Vx = V + M * t.x0;
+    // the grouped copy's rows start at x = -(NT - 1)
+    const float2* Vx = V + M * (t.x0 + (WIN == kGrouped ? NT - 1 : 0));
 #pragma unroll
     for (int b = 0; b < NT; ++b) {
         // the window shift depends on the y row only (plane strides keep the alignment)

@@ -215,7 +215,8 @@ __device__ __forceinline__ bool eval_fast(const Geom& g, const float2* __restric
 {
     FastTaps<NDIM, INTERP, DERIV> t;
     bool flip;
-    if (!fast_taps<NDIM, INTERP, DERIV>(g, R, (float)kx, (float)ky, t, flip)) return false;
+    if (!fast_taps<NDIM, INTERP, DERIV, WIN == kGrouped>(g, R, (float)kx, (float)ky, t, flip))
+        return false;
     gather_fast<NDIM, INTERP, WIN, DERIV>(V, t, v, dv);
     if (flip) {
         // v(c) = conj(v'(-c)); dv/dc = -conj(dv'/dc')
@@ -258,7 +259,8 @@ __global__ void __launch_bounds__(NDIM == 3 ? kFwd3Threads : kThreads, 4) projec
         ItemParams<NDIM> ip;
         load_item<NDIM>(g, rot, shift, ir.r, ir.p, ip);
         const float2* V = rec + (long long)ir.r * g.rec_elems;
-        const float2* VG = WIN == kGrouped ? grouped + (long long)Taps<INTERP>::N * ir.r * g.rec_elems : V;
+        const float2* VG =
+            WIN == kGrouped ? grouped + (long long)ir.r * g.Dv * g.gplane * Taps<INTERP>::N : V;
         float2* y = out + ir.item * g.img_elems;
         // pixels beyond the cutoff are zero
         for (int p = ir.part * BT + threadIdx.x; p < npix; p += splits * BT) {
@@ -421,7 +423,8 @@ __global__ void __launch_bounds__(kPoseThreads, 4) grad_pose_kernel(
         ItemParams<NDIM> ip;
         load_item<NDIM>(g, rot, shift, ir.r, ir.p, ip);
         const float2* V = rec + (long long)ir.r * g.rec_elems;
-        const float2* VG = WIN == kGrouped ? grouped + (long long)Taps<INTERP>::N * ir.r * g.rec_elems : V;
+        const float2* VG =
+            WIN == kGrouped ? grouped + (long long)ir.r * g.Dv * g.gplane * Taps<INTERP>::N : V;
         const float2* gy = gout + ir.item * g.img_elems;
         float acc[NG];
 #pragma unroll
@@ -1457,22 +1460,57 @@ LaunchShape launch_shape(const Geom& g, int sms)
     return s;
 }
 
-// Grouped copy of the volumes for the gathers: for every voxel (row, x) the NT taps
-// x .. x + NT - 1 of its row, zero past the stored half axis x = Dv/2.  Layout
-// [n_rec][Dv][Dv][Hv][NT] complex; a row's taps are then one aligned vector load.  One CTA
-// per volume row at a time, threads over the row's NT * Hv outputs (coalesced stores).
-template <int NT>
+// Grouped copy of the volumes for the gathers: for every volume row (z, y) and every group
+// start x = -(NT - 1) .. Dv/2 the NT taps x .. x + NT - 1 of the extended spectrum -- V[z][y][x]
+// for 0 <= x <= Dv/2, zero beyond, and for x < 0 the conjugate mirror conj V[-z][-y][-x]
+// (Friedel symmetry of the half spectrum; zero when -z or -y is outside the stored band or
+// -x > Dv/2), the value the per-tap rule reads there.  Group (z, y, x) sits at group index
+// z * pplane + y * prow + x + NT - 1 of its volume (pitches from group_pitch; the padding
+// groups are written as zeros), and a row's taps are then one aligned vector load.  A thread
+// per group (IDX: 32-bit index arithmetic when the groups fit, else 64-bit).
+template <int NT, typename IDX>
 __global__ void __launch_bounds__(kThreads) expand_groups_kernel(const float2* __restrict__ V,
-                                                                  float2* __restrict__ Q, int Hv,
-                                                                  int halfv, long long rows)
+                                                                  float2* __restrict__ Q, int Dv,
+                                                                  int Hv, int halfv, int centered,
+                                                                  int prow, int pplane,
+                                                                  IDX n_groups)
 {
-    for (long long row = blockIdx.x; row < rows; row += gridDim.x) {
-        const float2* v = V + row * Hv;
-        float2* q = Q + row * Hv * NT;
-        for (int e = threadIdx.x; e < Hv * NT; e += kThreads) {
-            const int x = e / NT, k = e - x * NT;
-            q[e] = x + k <= halfv ? __ldg(v + x + k) : make_float2(0.f, 0.f);
+    constexpr int LEAD = NT - 1;  // groups ahead of x = 0
+    const IDX P = (IDX)pplane, D = (IDX)Dv;
+    // consecutive threads write consecutive groups
+    for (IDX i = (IDX)blockIdx.x * kThreads + threadIdx.x; i < n_groups;
+         i += (IDX)gridDim.x * kThreads) {
+        const IDX zr = i / P;  // r * Dv + z
+        const int j = (int)(i - zr * P);
+        const int iy = j / prow;
+        const int x0 = j - iy * prow - LEAD;
+        float2 e[NT];
+#pragma unroll
+        for (int k = 0; k < NT; ++k) e[k] = make_float2(0.f, 0.f);
+        if (iy < Dv) {
+            const IDX r = zr / D;
+            const int iz = (int)(zr - r * D);
+            const float2* v = V + ((long long)zr * Dv + iy) * Hv;
+            const float2* vm = nullptr;  // the mirrored row (-z, -y), when x0 < 0
+            if (x0 < 0) {
+                const int iym = full_index(-row_freq(iy, Dv, halfv, centered), Dv, halfv, centered);
+                const int izm = full_index(-row_freq(iz, Dv, halfv, centered), Dv, halfv, centered);
+                if ((iym | izm) >= 0) vm = V + (((long long)r * Dv + izm) * Dv + iym) * Hv;
+            }
+#pragma unroll
+            for (int k = 0; k < NT; ++k) {
+                const int x = x0 + k;
+                if (x >= 0) {
+                    if (x <= halfv) e[k] = __ldg(v + x);
+                } else if (vm && -x <= halfv) {
+                    e[k] = __ldg(vm - x);
+                    e[k].y = -e[k].y;
+                }
+            }
         }
+        float4* q = reinterpret_cast<float4*>(Q + (long long)i * NT);
+#pragma unroll
+        for (int k = 0; k < NT; k += 2) q[k / 2] = make_float4(e[k].x, e[k].y, e[k + 1].x, e[k + 1].y);
     }
 }
 
@@ -1696,15 +1734,25 @@ cudaError_t launch_weights_grad(int ndim, int interp, const Geom& g, const float
 cudaError_t launch_expand_groups(int interp, const Geom& g, const void* rec, void* grouped, int sms,
                                  cudaStream_t stream)
 {
-    const long long rows = (long long)g.n_rec * g.Dv * g.Dv;
-    if (rows == 0) return cudaSuccess;
-    const unsigned grid = (unsigned)(rows < 16LL * sms ? rows : 16LL * sms);
+    const long long n_groups = (long long)g.n_rec * g.Dv * g.gplane;
+    if (n_groups == 0) return cudaSuccess;
+    const long long blocks = (n_groups + kThreads - 1) / kThreads;
+    const unsigned grid = (unsigned)(blocks < 64LL * sms ? blocks : 64LL * sms);
     auto V = static_cast<const float2*>(rec);
     auto Q = static_cast<float2*>(grouped);
-    if (interp == kCubic)
-        expand_groups_kernel<4><<<grid, kThreads, 0, stream>>>(V, Q, g.Hv, g.halfv, rows);
+    const bool narrow = n_groups < (1LL << 31);  // 32-bit index arithmetic
+    if (interp == kCubic && narrow)
+        expand_groups_kernel<4, unsigned><<<grid, kThreads, 0, stream>>>(
+            V, Q, g.Dv, g.Hv, g.halfv, g.centered, g.grow, g.gplane, (unsigned)n_groups);
+    else if (interp == kCubic)
+        expand_groups_kernel<4, long long><<<grid, kThreads, 0, stream>>>(
+            V, Q, g.Dv, g.Hv, g.halfv, g.centered, g.grow, g.gplane, n_groups);
+    else if (narrow)
+        expand_groups_kernel<2, unsigned><<<grid, kThreads, 0, stream>>>(
+            V, Q, g.Dv, g.Hv, g.halfv, g.centered, g.grow, g.gplane, (unsigned)n_groups);
     else
-        expand_groups_kernel<2><<<grid, kThreads, 0, stream>>>(V, Q, g.Hv, g.halfv, rows);
+        expand_groups_kernel<2, long long><<<grid, kThreads, 0, stream>>>(
+            V, Q, g.Dv, g.Hv, g.halfv, g.centered, g.grow, g.gplane, n_groups);
     return cudaGetLastError();
 }
 

@@ -20,7 +20,8 @@ cudaError_t launch_backward(int ndim, int interp, const Geom& g, const void* rec
                             void* grad_rec, float* grad_rot, float* grad_shift, int sms,
                             cudaStream_t stream, const void* grouped = nullptr);
 
-// Grouped copy of the volumes: [n_rec][Dv][Dv][Hv][NT] complex, NT = 4 (cubic) / 2 (linear).
+// Grouped copy of the volumes for the gathers: n_rec * Dv * g.gplane groups of NT complex taps,
+// NT = 4 (cubic) / 2 (linear); see expand_groups_kernel.
 cudaError_t launch_expand_groups(int interp, const Geom& g, const void* rec, void* grouped, int sms,
                                  cudaStream_t stream);
 

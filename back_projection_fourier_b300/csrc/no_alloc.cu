@@ -12,11 +12,12 @@
 #include <mutex>
 
 #include "../../include/tp.h"
+#include "tp_device.cuh"
 
 namespace {
 
-// One D = 128 volume with cubic taps: 128 * 128 * 65 voxels * 4 taps * 8 bytes.
-constexpr size_t kScratchBytes = 34078720;
+// The grouped copy of one D = 128 volume with cubic taps.
+constexpr size_t kScratchBytes = (size_t)tp::grouped_volume_elems(128, 4) * 8;
 static __device__ __align__(256) unsigned char g_scratch[kScratchBytes];
 
 constexpr int kMaxDevices = 64;

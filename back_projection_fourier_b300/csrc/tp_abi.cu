@@ -81,6 +81,9 @@ tp::Geom make_geom(int ndim, int n_rec, int Dv, int n_rot, int n_pose, const flo
     g.rc2 = rc2 >= (double)INT_MAX ? INT_MAX : (int)rc2;
     g.rec_elems = ndim == 3 ? (long long)Dv * Dv * g.Hv : (long long)Dv * g.Hv;
     g.img_elems = (long long)Do * g.Ho;
+    const tp::GroupPitch gp = tp::group_pitch(Dv, o.interp == TP_CUBIC ? 4 : 2);
+    g.grow = gp.row;
+    g.gplane = gp.plane;
     return g;
 }
 
@@ -98,7 +101,7 @@ size_t grouped_bytes(int ndim, int n_rec, int Dv, int interp)
 {
     if (ndim != 3 || n_rec <= 0 || !box_ok(Dv, 3)) return 0;
     const long long nt = interp == TP_CUBIC ? 4 : 2;
-    const long long per = (long long)Dv * Dv * (Dv / 2 + 1) * nt;
+    const long long per = tp::grouped_volume_elems(Dv, (int)nt);
     if (per >= (1LL << 31)) return 0;
     if ((long long)n_rec > (LLONG_MAX / 8) / per) return 0;  // beyond any device memory
     return (size_t)(per * n_rec * 8);

@@ -27,6 +27,42 @@ struct Taps {
     static constexpr int first = INTERP == kCubic ? -1 : 0;  // first tap relative to floor(c)
 };
 
+// Pitches of the gathers' grouped copy of a 3D volume, in groups of NT taps (8 NT bytes).
+// A row holds at least Hv + NT - 1 groups (starts x = -(NT - 1) .. Dv/2) and a plane at least
+// Dv rows.  Each is padded up to a fixed residue modulo the groups in a 128-byte line
+// (16 / NT): the residues set where the y and z neighbours of a tap row fall within their
+// cache lines, and so how the rows that the lanes of a warp load spread over the L1 data
+// banks.  Measured at D = 128, cubic, 16 384 poses (forward + pose gradients): residues
+// (row, plane) = (2, 1) 9.50 ms, (1, 2) 9.52, (1, 0) 10.14, (0, 0) -- every row starting a
+// cache line -- 10.88.
+#ifndef TP_GROUP_ROW_RES
+#define TP_GROUP_ROW_RES 2
+#endif
+#ifndef TP_GROUP_PLANE_RES
+#define TP_GROUP_PLANE_RES 1
+#endif
+struct GroupPitch {
+    int row, plane;
+};
+
+__host__ __device__ constexpr int pad_to_residue(int n, int m, int res)
+{
+    return n + ((res - n) % m + m) % m;
+}
+
+__host__ __device__ constexpr GroupPitch group_pitch(int Dv, int nt)
+{
+    return {pad_to_residue(Dv / 2 + nt, 16 / nt, TP_GROUP_ROW_RES),
+            pad_to_residue(Dv * pad_to_residue(Dv / 2 + nt, 16 / nt, TP_GROUP_ROW_RES), 16 / nt,
+                           TP_GROUP_PLANE_RES)};
+}
+
+// Complex elements of one volume's grouped copy.
+__host__ __device__ constexpr long long grouped_volume_elems(int Dv, int nt)
+{
+    return (long long)Dv * group_pitch(Dv, nt).plane * nt;
+}
+
 // Launch-wide geometry of one call, passed by value.
 struct Geom {
     int n_rec, n_pose;
@@ -41,6 +77,7 @@ struct Geom {
     int rc2;                    // keep pixel iff kx^2 + ky^2 <= rc2 (integer)
     long long rec_elems;        // elements of one reconstruction
     long long img_elems;        // elements of one image (Do * Ho)
+    int grow, gplane;           // grouped copy (3D): group_pitch(Dv, NT of the call)
 };
 
 // ---------------------------------------------------------------- indexing -----
@@ -96,16 +133,22 @@ __device__ __forceinline__ dfloat dot2(float r0, float x, float r1, float y)
     return {s.hi, __fadd_rn(__fadd_rn(p.lo, q.lo), s.lo)};
 }
 
-// floor and fraction of hi + lo (optionally scaled by o first).  frac is in [0, 1]; the
-// value 1 can only come from rounding of an fp32 fraction just below 1, and both the
-// kernels and their derivatives are continuous there (cubic) or take the neighbouring
-// cell's value (linear), so either reading samples the same interpolant.
-__device__ __forceinline__ void floor_frac(dfloat c, float o, int o_is_one, int& base, float& frac)
+// o * (hi + lo) as hi + lo (exact up to the rounding of the low part); c itself when o = 1.
+__device__ __forceinline__ dfloat scale_coord(dfloat c, float o, int o_is_one)
 {
     if (!o_is_one) {
         const dfloat h = two_prod(o, c.hi);
         c = {h.hi, __fmaf_rn(o, c.lo, h.lo)};
     }
+    return c;
+}
+
+// floor and fraction of hi + lo (already scaled).  frac is in [0, 1]; the value 1 can only
+// come from rounding of an fp32 fraction just below 1, and both the kernels and their
+// derivatives are continuous there (cubic) or take the neighbouring cell's value (linear),
+// so either reading samples the same interpolant.
+__device__ __forceinline__ void floor_split(dfloat c, int& base, float& frac)
+{
     // Beyond +-2^23 every tap lies outside any supported box; clamping keeps the integer
     // tap indices far from overflow for any input (a NaN coordinate clamps too, and its
     // NaN weights propagate to the output without touching memory out of range).
@@ -121,6 +164,12 @@ __device__ __forceinline__ void floor_frac(dfloat c, float o, int o_is_one, int&
     }
     base = (int)fl;
     frac = fr;
+}
+
+// floor and fraction of o * (hi + lo).
+__device__ __forceinline__ void floor_frac(dfloat c, float o, int o_is_one, int& base, float& frac)
+{
+    floor_split(scale_coord(c, o, o_is_one), base, frac);
 }
 
 // ----------------------------------------------------------------- weights -----
@@ -268,10 +317,12 @@ __device__ __forceinline__ void gather(const float2* __restrict__ V, const Geom&
     if constexpr (DERIV) {
         dv[0] = dv[1] = dv[2] = make_float2(0.f, 0.f);
     }
+    // y rows outer, z planes inner: the order of the fast path's gather_fast, so a pixel
+    // gives the same bits on either path when both read the same tap values
 #pragma unroll
-    for (int a = 0; a < NZ; ++a) {
+    for (int b = 0; b < NT; ++b) {
 #pragma unroll
-        for (int b = 0; b < NT; ++b) {
+        for (int a = 0; a < NZ; ++a) {
             const int rd = t.row(g, a, b, false);
             const int rm = t.row(g, a, b, true);
             float2 rs = make_float2(0.f, 0.f), rsd = make_float2(0.f, 0.f);

@@ -141,14 +141,18 @@ tp_status tp_project_backward(int ndim, const void* rec, int n_rec, int Dv, cons
 /* Optional workspace of the 3D gathers.  tp_project_3d_to_2d_ws and tp_project_backward_ws
  * are tp_project_3d_to_2d and tp_project_backward with a caller-owned device workspace; the
  * results are the same (the same taps, weights and summation order).  The call first writes
- * a grouped copy of the volumes into the workspace -- for every voxel the NT taps x .. x+NT-1
- * of its row, NT = 4 (cubic) or 2 (linear), zeros past x = Dv/2, layout
- * [n_rec][Dv][Dv][Dv/2+1][NT] complex -- and the gathers then read each row of taps with
- * one aligned vector load instead of several unaligned ones.  It costs NT times the volumes'
+ * a grouped copy of the volumes into the workspace -- for every row and every start
+ * x = -(NT-1) .. Dv/2 the NT taps x .. x+NT-1 of that row, NT = 4 (cubic) or 2 (linear),
+ * zeros past x = Dv/2 and the conjugate Friedel mirror left of x = 0 -- and the gathers then
+ * read each row of taps with one aligned vector load instead of several unaligned ones, also
+ * for the pixels whose taps straddle the x = 0 plane.  Layout: per volume Dv planes of P
+ * groups, a plane holding Dv rows of R groups, a group NT complex values; R = Dv/2 + NT
+ * padded up to 2 modulo 16/NT and P = Dv * R padded up to 1 modulo 16/NT (padding that
+ * spreads the rows a warp loads over the L1 banks).  It costs about NT times the volumes'
  * memory and one pass over them per call; it pays when many poses share the volumes.
  * This is a B300 layout choice; the pages have no counterpart.
  *
- * tp_workspace_size returns the bytes needed (n_rec * Dv * Dv * (Dv/2+1) * NT * 8), or 0
+ * tp_workspace_size returns the bytes needed (n_rec * Dv * P * NT * 8), or 0
  * when the workspace would not be used (ndim = 2, invalid sizes or options, or NT times one
  * volume's elements >= 2^31).  A NULL workspace runs the plain path; so does any workspace
  * when tp_workspace_size is 0 for these arguments (the workspace is then ignored).
@@ -175,9 +179,9 @@ tp_status tp_project_backward_ws(int ndim, const void* rec, int n_rec, int Dv, c
  * latency-critical path that must not call cudaMalloc, which can synchronise the device.
  * The pages have no counterpart; this is a property of the library, not of the method.
  *   Arguments, layouts and results as tp_project_3d_to_2d.  The grouped copy of the volumes
- *   goes into a fixed scratch array of 34078720 bytes (one Dv = 128 volume with cubic taps)
+ *   goes into a fixed scratch array of 36704256 bytes (one Dv = 128 volume with cubic taps)
  *   that the library holds in device memory on every GPU that loads it, until the process
- *   exits.  Sizes whose grouped copy needs more (tp_workspace_size above 34078720) return
+ *   exits.  Sizes whose grouped copy needs more (tp_workspace_size above 36704256) return
  *   TP_ERR_SHAPE before anything is enqueued.  The call allocates nothing.
  *   The first call on a device, with that device current, looks up the array's device
  *   address (cudaGetSymbolAddress) and keeps it, per process and per device ordinal, for

@@ -139,15 +139,20 @@ def test_pad_argument_errors(fn):
 
 
 def test_workspace_size():
-    assert tp.tp_workspace_size(3, 1, 128, tp.make_opts(1)) == 128 * 128 * 65 * 4 * 8
-    assert tp.tp_workspace_size(3, 2, 64, tp.make_opts(0)) == 2 * 64 * 64 * 33 * 2 * 8
+    # cubic D = 128: rows of 64 + 4 = 68 groups padded to 70 (2 mod 4), planes of 128 * 70
+    # groups padded to 8961 (1 mod 4), 4 taps of 8 bytes a group
+    assert tp.tp_workspace_size(3, 1, 128, tp.make_opts(1)) == 128 * 8961 * 4 * 8
+    # linear D = 64: rows of 32 + 2 = 34 groups (already 2 mod 8), planes of 64 * 34 = 2176
+    # groups padded to 2177 (1 mod 8), 2 taps a group
+    assert tp.tp_workspace_size(3, 2, 64, tp.make_opts(0)) == 2 * 64 * 2177 * 2 * 8
     assert tp.tp_workspace_size(2, 1, 128, tp.make_opts(1)) == 0      # 2D: not used
     assert tp.tp_workspace_size(3, 1, 7, tp.make_opts(1)) == 0        # odd box
     assert tp.tp_workspace_size(3, 1, 1024, tp.make_opts(1)) == 0     # 32-bit offsets
     assert tp.tp_workspace_size(3, 1, 128, tp.make_opts(5)) == 0      # bad interp
-    per = 1022 * 1022 * 512 * 4 * 8                                   # bytes of one volume's copy
-    assert tp.tp_workspace_size(3, 2**29, 1022, tp.make_opts(1)) == per * 2**29
-    assert tp.tp_workspace_size(3, 2**31 - 1, 1022, tp.make_opts(1)) == 0   # would overflow
+    per = 1020 * (1020 * 514 + 1) * 4 * 8                             # bytes of one volume's copy
+    assert tp.tp_workspace_size(3, 2**29, 1020, tp.make_opts(1)) == per * 2**29
+    assert tp.tp_workspace_size(3, 1, 1022, tp.make_opts(1)) == 0     # 32-bit offsets: just over
+    assert tp.tp_workspace_size(3, 2**31 - 1, 1020, tp.make_opts(1)) == 0   # would overflow
     assert tp.tp_workspace_size(3, -1, 128, tp.make_opts(1)) == 0
 
 
@@ -301,7 +306,7 @@ int main(void) {{
     assert out[0].startswith("TP_ERR_SHAPE")
     assert out[1] == "2"                    # odd volume box
     assert out[2] == "1"                    # valid sizes, one item, NULL pointers: TP_ERR_NULL
-    assert out[3] == str(128 * 128 * 65 * 4 * 8)
+    assert out[3] == str(128 * 8961 * 4 * 8)
     assert out[4] == str(len(tp.header_symbols()))
 
 

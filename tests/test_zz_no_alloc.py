@@ -17,7 +17,7 @@ from back_projection_fourier_b300 import synth, tp
 pytestmark = pytest.mark.gpu
 
 TOL_FWD = 1e-5       # the forward projection's parity bar
-SCRATCH_BYTES = 34078720
+SCRATCH_BYTES = 36704256
 
 
 def max_rel(a, b):
