@@ -908,26 +908,47 @@ constexpr int kTilePix = 16;                        // 4 x 4 pixels
 // One record per pixel, stored contiguously (array of structs): gx gy wt base (one 16-byte
 // broadcast load) | wx[4] | wy[4] | wz in the order 0, 2, 1, 3, so that the z weights of a
 // lane's two planes a and a + 2 are one 8-byte load (the tap loop forms wz * wy) | fx fy fz.
-// base < 0 flags the per-tap path and holds ~base.
-struct TileRec {
-    static constexpr int GX = 0, GY = 1, WT = 2, BASE = 3, WX = 4, WY = 8, WZ = 12;
-    static constexpr int FX = 16, FY = 17, FZ = 18;
-    static constexpr int STRIDE = 20;                // 16-byte aligned records
-    static constexpr int WORDS = STRIDE * kTilePix;  // a multiple of 4: 16-byte aligned records
+// base < 0 flags the per-tap path and holds ~base.  With the pose gradients (POSE) the record
+// also holds the derivative weights (z in the order 0, 2, 1, 3) and, for reading the volume at
+// the taps, the element offset iy * Hv + x0 of each y tap row and iz * Dv * Hv of each z tap
+// plane (order 0, 2, 1, 3), kOutside when the tap lies outside the stored band.
+template <bool POSE>
+struct TileRecT {
+    enum : int { GX = 0, GY = 1, WT = 2, BASE = 3, WX = 4, WY = 8, WZ = 12, FX = 16, FY = 17, FZ = 18 };
+    enum : int { DWX = 20, DWY = 24, DWZ = 28, YO = 32, ZO = 36 };
+    enum : int {
+        STRIDE = POSE ? 40 : 20,    // 16-byte aligned records
+        WORDS = STRIDE * kTilePix,  // a multiple of 4: 16-byte aligned records
+    };
 };
+using TileRec = TileRecT<false>;
+// Offset of a tap row or plane outside the stored band: any sum of offsets that includes it
+// stays negative (valid offsets are below 2^30 for every supported box).
+constexpr int kOutside = -(1 << 30);
+// CTAs of the fused backward (volume and pose gradients): 6 warps, whose larger records still
+// let four CTAs fit in shared memory.
+constexpr int kTileThreadsPose = 192;
 
-template <int INTERP, bool DATA, bool WTS>
-__global__ void __launch_bounds__(kTileThreads) scatter_tile_kernel(
-    const float2* __restrict__ proj, const float* __restrict__ wts,
-    const float* __restrict__ rot, const float* __restrict__ shift,
-    float2* __restrict__ vout, float* __restrict__ wout, Geom g, int splits, long long n_work)
+// POSE: the fused backward.  Besides the volume gradient the kernel forms the rotation and
+// shift gradients: every lane reads the volume at its two taps of the pixel (effective frame,
+// the exact Friedel rule on the per-tap path), and accumulates, over the item's pixels, the
+// terms o q_b Re(conj(g') dv/dc_a) and (2 pi / Do) q_b Im(conj(g') v) of each tap; a warp
+// reduction and one atomic per term per warp finish the item.
+template <int INTERP, bool DATA, bool WTS, bool POSE = false>
+__global__ void __launch_bounds__(POSE ? kTileThreadsPose : kTileThreads, POSE ? 4 : 0)
+scatter_tile_kernel(const float2* __restrict__ proj, const float* __restrict__ wts,
+                    const float* __restrict__ rot, const float* __restrict__ shift,
+                    float2* __restrict__ vout, float* __restrict__ wout, Geom g, int splits,
+                    long long n_work, const float2* __restrict__ vol = nullptr,
+                    float* __restrict__ grot = nullptr, float* __restrict__ gsh = nullptr)
 {
     static_assert(INTERP == kCubic, "the linear 3D scatter is scatter_lane_kernel");
-    using TR = TileRec;
+    static_assert(!POSE || (DATA && !WTS), "the fused backward scatters data only");
+    using TR = TileRecT<POSE>;
     constexpr int NT = Taps<INTERP>::N;
     constexpr int FIRST = Taps<INTERP>::first;
     constexpr int TPL = 2;                 // taps per lane: 64 taps on 32 lanes
-    constexpr int NWARP = kTileThreads / 32;
+    constexpr int NWARP = (POSE ? kTileThreadsPose : kTileThreads) / 32;
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     extern __shared__ __align__(16) unsigned char sm_raw[];
     using BX = BoxDims<WTS>;
@@ -978,6 +999,12 @@ __global__ void __launch_bounds__(kTileThreads) scatter_tile_kernel(
         const float* pw = (WTS && wts) ? wts + ir.item * g.img_elems : nullptr;  // NULL: weight 1
         float2* G = DATA ? vout + (long long)ir.r * g.rec_elems : nullptr;
         float* Wt = WTS ? wout + (long long)ir.r * g.rec_elems : nullptr;
+        const float2* V = POSE ? vol + (long long)ir.r * g.rec_elems : nullptr;
+        // pose-gradient terms of this lane: o-free d/dR[a][b] (a = x, y, z; b = kx, ky) and
+        // the shift's two
+        float pacc[POSE ? 8 : 1];
+#pragma unroll
+        for (int k = 0; k < (POSE ? 8 : 1); ++k) pacc[k] = 0.f;
 
         for (int tile = ir.part * NWARP + warp; tile < ntiles; tile += splits * NWARP) {
             const int ti = tile / tiles_x, tj = tile - ti * tiles_x;
@@ -1048,10 +1075,33 @@ __global__ void __launch_bounds__(kTileThreads) scatter_tile_kernel(
                     rf[TR::GX] = gp.x;
                     rf[TR::GY] = sg * gp.y;
                     const int base = ((fz + FIRST - z0) * NY + (fy + FIRST - y0)) * PITCH + (fx + FIRST - x0);
-                    ri[TR::BASE] = (fx + FIRST <= 0 || !boxed) ? ~base : base;
+                    // (POSE: taps past x = Dv/2 also take the per-tap path, where the volume
+                    // reads follow the exact rule)
+                    ri[TR::BASE] = (fx + FIRST <= 0 || !boxed || (POSE && fx + FIRST + NT - 1 > g.halfv))
+                                       ? ~base
+                                       : base;
                     ri[TR::FX] = fx;
                     ri[TR::FY] = fy;
                     ri[TR::FZ] = fz;
+                    if constexpr (POSE) {
+                        float dx_[NT], dy_[NT], dz_[NT];
+                        dweights<INTERP>(ex - flx, dx_);
+                        dweights<INTERP>(ey - fly, dy_);
+                        dweights<INTERP>(ez - flz, dz_);
+                        *reinterpret_cast<float4*>(rf + TR::DWX) = make_float4(dx_[0], dx_[1], dx_[2], dx_[3]);
+                        *reinterpret_cast<float4*>(rf + TR::DWY) = make_float4(dy_[0], dy_[1], dy_[2], dy_[3]);
+                        *reinterpret_cast<float4*>(rf + TR::DWZ) = make_float4(dz_[0], dz_[2], dz_[1], dz_[3]);
+                        int yo[NT], zo[NT];
+#pragma unroll
+                        for (int k = 0; k < NT; ++k) {
+                            const int iy = full_index(fy + FIRST + k, g.Dv, g.halfv, g.centered);
+                            const int iz = full_index(fz + FIRST + k, g.Dv, g.halfv, g.centered);
+                            yo[k] = iy < 0 ? kOutside : iy * g.Hv + fx + FIRST;
+                            zo[k] = iz < 0 ? kOutside : iz * g.Dv * g.Hv;
+                        }
+                        *reinterpret_cast<int4*>(ri + TR::YO) = make_int4(yo[0], yo[1], yo[2], yo[3]);
+                        *reinterpret_cast<int4*>(ri + TR::ZO) = make_int4(zo[0], zo[2], zo[1], zo[3]);
+                    }
                 }
                 __syncwarp();
                 int toff[TPL];
@@ -1073,7 +1123,16 @@ __global__ void __launch_bounds__(kTileThreads) scatter_tile_kernel(
                         const float2 zp = *reinterpret_cast<const float2*>(rf + TR::WZ + 2 * ta[0]);
                         const float wyb = rf[TR::WY + tb[0]];
                         const float wzy[TPL] = {zp.x * wyb, zp.y * wyb};
+                        float2 vv[POSE ? TPL : 1];  // the volume at this lane's taps (POSE)
                         if (rb >= 0) {
+                            if constexpr (POSE) {
+                                // taps at 1 <= x <= Dv/2: direct reads, zero outside the band
+                                const int yo = ri[TR::YO + tb[0]];
+                                const int2 zo = *reinterpret_cast<const int2*>(ri + TR::ZO + 2 * ta[0]);
+                                const int o0 = zo.x + yo + tk, o1 = zo.y + yo + tk;
+                                vv[0] = o0 >= 0 ? __ldg(V + o0) : make_float2(0.f, 0.f);
+                                vv[1] = o1 >= 0 ? __ldg(V + o1) : make_float2(0.f, 0.f);
+                            }
 #pragma unroll
                             for (int m = 0; m < TPL; ++m) {
                                 const float w = wzy[m] * wxk;
@@ -1096,6 +1155,22 @@ __global__ void __launch_bounds__(kTileThreads) scatter_tile_kernel(
                                 const float w = wzy[m] * wxk;
                                 const int ux = pfx + FIRST + tk;
                                 const bool direct = ux >= 1 || (ux == 0 && pass == 0);
+                                if constexpr (POSE) {
+                                    // the value of the extended spectrum at this tap
+                                    int vx = ux, vy = pfy + FIRST + tb[m], vz = pfz + FIRST + ta[m];
+                                    if (!direct) {
+                                        vx = -vx;
+                                        vy = -vy;
+                                        vz = -vz;
+                                    }
+                                    const int iy = full_index(vy, g.Dv, g.halfv, g.centered);
+                                    const int iz = full_index(vz, g.Dv, g.halfv, g.centered);
+                                    float2 val = make_float2(0.f, 0.f);
+                                    if (vx >= 0 && vx <= g.halfv && iy >= 0 && iz >= 0)
+                                        val = __ldg(V + ((long long)iz * g.Dv + iy) * g.Hv + vx);
+                                    if (!direct) val.y = -val.y;
+                                    vv[m] = val;
+                                }
                                 if (direct && boxed) {
                                     const int e = base + toff[m];
                                     if (DATA) {
@@ -1124,6 +1199,37 @@ __global__ void __launch_bounds__(kTileThreads) scatter_tile_kernel(
                                     }
                                 }
                             }
+                        }
+                        if constexpr (POSE) {
+                            // this lane's share of Re(conj(h) dv'/dc'_a) and Im(conj(h) v') (h
+                            // the record's value, v' the effective-frame sample; separable
+                            // weights), times q_b and the pass sign (dv/dc = -conj(dv'/dc'),
+                            // v = conj(v') on the mirrored pass)
+                            const float dwxk = rf[TR::DWX + tk];
+                            const float dwyb = rf[TR::DWY + tb[0]];
+                            const float2 dzp = *reinterpret_cast<const float2*>(rf + TR::DWZ + 2 * ta[0]);
+                            float tre[TPL], tim[TPL];
+#pragma unroll
+                            for (int m = 0; m < TPL; ++m) {
+                                tre[m] = fmaf(gv.x, vv[m].x, gv.y * vv[m].y);
+                                tim[m] = fmaf(gv.x, vv[m].y, -gv.y * vv[m].x);
+                            }
+                            const float za = fmaf(zp.x, tre[0], zp.y * tre[1]);
+                            const float zd = fmaf(dzp.x, tre[0], dzp.y * tre[1]);
+                            const float zi = fmaf(zp.x, tim[0], zp.y * tim[1]);
+                            const float wyx = wyb * wxk;
+                            const float sx = wyb * dwxk * za, sy = dwyb * wxk * za;
+                            const float sz = wyx * zd, ss = wyx * zi;
+                            const float qx = sg * (float)(4 * tj + (j & 3));
+                            const float qy = sg * (float)row_freq(4 * ti + (j >> 2), g.Do, g.halfo, g.centered);
+                            pacc[0] = fmaf(sx, qx, pacc[0]);
+                            pacc[1] = fmaf(sx, qy, pacc[1]);
+                            pacc[2] = fmaf(sy, qx, pacc[2]);
+                            pacc[3] = fmaf(sy, qy, pacc[3]);
+                            pacc[4] = fmaf(sz, qx, pacc[4]);
+                            pacc[5] = fmaf(sz, qy, pacc[5]);
+                            pacc[6] = fmaf(ss, qx, pacc[6]);
+                            pacc[7] = fmaf(ss, qy, pacc[7]);
                         }
                     }
                     __syncwarp();
@@ -1174,6 +1280,29 @@ __global__ void __launch_bounds__(kTileThreads) scatter_tile_kernel(
                     }
                 }
                 __syncwarp();
+            }
+        }
+        if constexpr (POSE) {
+            // the warp's sums for this item: one atomic per term
+#pragma unroll
+            for (int k = 0; k < 8; ++k) {
+                float v = pacc[k];
+#pragma unroll
+                for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+                pacc[k] = v;
+            }
+            if (lane == 0) {
+                const long long ri = (long long)(g.rot_shared ? 0 : ir.r) * g.n_pose + ir.p;
+                const long long si = (long long)(g.sh_shared ? 0 : ir.r) * g.n_pose + ir.p;
+                if (grot) {
+#pragma unroll
+                    for (int k = 0; k < 6; ++k) atomicAdd(grot + ri * 9 + (k / 2) * 3 + (k % 2), g.o * pacc[k]);
+                }
+                if (gsh && g.has_shift) {
+                    const float two_pi_over_Do = 6.283185307179586f * g.inv_Do;
+                    atomicAdd(gsh + si * 2, two_pi_over_Do * pacc[6]);
+                    atomicAdd(gsh + si * 2 + 1, two_pi_over_Do * pacc[7]);
+                }
             }
         }
     }
@@ -1627,16 +1756,17 @@ void launch_scatter_rows(const Geom& g, const float2* P, const float* weights, c
     kern<<<grid, kRowsThreads, smem, stream>>>(P, weights, rot, shift, VO, WO, g, n_items);
 }
 
-template <int INTERP, bool DATA, bool WTS>
-void launch_scatter_tile(const Geom& g, const float2* P, const float* weights, const float* rot,
-                         const float* shift, float2* VO, float* WO, int sms, cudaStream_t stream)
+template <int INTERP, bool DATA, bool WTS, bool POSE>
+void launch_scatter_tile_t(const Geom& g, const float2* P, const float* weights, const float* rot,
+                           const float* shift, float2* VO, float* WO, int sms, cudaStream_t stream,
+                           const float2* vol, float* grot, float* gsh)
 {
     constexpr size_t box_cap = BoxDims<WTS>::CAP;
     const size_t per_warp = (DATA ? box_cap * 8 : 0) + (WTS ? box_cap * 4 : 0) +
-                            (size_t)TileRec::WORDS * 4;
-    constexpr int threads = kTileThreads, nwarp = threads / 32;
+                            (size_t)TileRecT<POSE>::WORDS * 4;
+    constexpr int threads = POSE ? kTileThreadsPose : kTileThreads, nwarp = threads / 32;
     const size_t smem = per_warp * nwarp;
-    auto kern = scatter_tile_kernel<INTERP, DATA, WTS>;
+    auto kern = scatter_tile_kernel<INTERP, DATA, WTS, POSE>;
     cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     const long long n_items = (long long)g.n_rec * g.n_pose;
     const long long ntiles = (long long)((g.Ho + 3) / 4) * ((g.Do + 3) / 4);
@@ -1644,7 +1774,16 @@ void launch_scatter_tile(const Geom& g, const float2* P, const float* weights, c
     const long long n_work = n_items * splits;
     const long long cap = 8LL * sms;
     const unsigned grid = (unsigned)(n_work < cap ? n_work : cap);
-    kern<<<grid, threads, smem, stream>>>(P, weights, rot, shift, VO, WO, g, splits, n_work);
+    kern<<<grid, threads, smem, stream>>>(P, weights, rot, shift, VO, WO, g, splits, n_work, vol,
+                                          grot, gsh);
+}
+
+template <int INTERP, bool DATA, bool WTS>
+void launch_scatter_tile(const Geom& g, const float2* P, const float* weights, const float* rot,
+                         const float* shift, float2* VO, float* WO, int sms, cudaStream_t stream)
+{
+    launch_scatter_tile_t<INTERP, DATA, WTS, false>(g, P, weights, rot, shift, VO, WO, sms, stream,
+                                                    nullptr, nullptr, nullptr);
 }
 
 template <bool DATA, bool WTS>
@@ -1778,7 +1917,7 @@ cudaError_t launch_project(int ndim, int interp, const Geom& g, const void* rec,
 cudaError_t launch_backward(int ndim, int interp, const Geom& g, const void* rec,
                             const float* rot, const float* shift, const void* grad_out,
                             void* grad_rec, float* grad_rot, float* grad_shift, int sms,
-                            cudaStream_t stream, const void* grouped)
+                            cudaStream_t stream, const void* grouped, bool fused)
 {
     if ((long long)g.n_rec * g.n_pose == 0) return cudaSuccess;
     auto R = static_cast<const float2*>(rec);
@@ -1786,6 +1925,12 @@ cudaError_t launch_backward(int ndim, int interp, const Geom& g, const void* rec
     auto GR = static_cast<float2*>(grad_rec);
     auto Q = static_cast<const float2*>(grouped);
     const bool want_grad = grad_rot || (grad_shift && g.has_shift);
+    if (fused && ndim == 3 && interp == kCubic && GR && want_grad) {
+        // one pass: volume, rotation and shift gradients
+        launch_scatter_tile_t<kCubic, true, false, true>(g, G, nullptr, rot, shift, GR, nullptr, sms,
+                                                         stream, R, grad_rot, grad_shift);
+        return cudaGetLastError();
+    }
     if (want_grad) {
         if (ndim == 3 && interp == kCubic)
             launch_grad_t<3, kCubic>(g, R, rot, shift, G, grad_rot, grad_shift, Q, sms, stream);

@@ -15,10 +15,13 @@ cudaError_t launch_project(int ndim, int interp, const Geom& g, const void* rec,
                            const float* rot, const float* shift, void* out, int sms,
                            cudaStream_t stream, const void* grouped = nullptr);
 
+// fused: the volume, rotation and shift gradients in one pass of the tile scatter where that
+// kernel applies (3D cubic, every output wanted); elsewhere the two kernels as without it.
 cudaError_t launch_backward(int ndim, int interp, const Geom& g, const void* rec,
                             const float* rot, const float* shift, const void* grad_out,
                             void* grad_rec, float* grad_rot, float* grad_shift, int sms,
-                            cudaStream_t stream, const void* grouped = nullptr);
+                            cudaStream_t stream, const void* grouped = nullptr,
+                            bool fused = false);
 
 // Grouped copy of the volumes for the gathers: n_rec * Dv * g.gplane groups of NT complex taps,
 // NT = 4 (cubic) / 2 (linear); see expand_groups_kernel.

@@ -182,6 +182,54 @@ tp_status backproject_impl(int ndim, const void* proj, const float* weights, int
     return e == cudaSuccess ? TP_OK : TP_ERR_CUDA;
 }
 
+// The backward of the projection; `fused` selects the one-pass kernel where it exists.
+tp_status project_backward_impl(int ndim, const void* rec, int n_rec, int Dv, const float* rot,
+                                int n_rot, int n_pose, const float* shift, int n_sh,
+                                const void* grad_out, int Do, void* grad_rec, float* grad_rot,
+                                float* grad_shift, void* workspace, size_t workspace_bytes,
+                                const tp_opts* opts, void* stream, bool fused)
+{
+    Opts o;
+    tp_status st = read_opts(opts, o);
+    if (st != TP_OK) return st;
+    st = check_common(ndim, n_rec, Dv, Do, n_rot, n_pose, shift, n_sh);
+    if (st != TP_OK) return st;
+    bool use_ws = false;
+    st = check_workspace(ndim, n_rec, Dv, o.interp, workspace, workspace_bytes, use_ws);
+    if (st != TP_OK) return st;
+    const long long n_items = (long long)n_rec * n_pose;
+    const bool want_grad = grad_rot || (grad_shift && shift);
+    if (n_items > 0 && (grad_rec || want_grad)) {
+        if (!grad_out || !rot || (want_grad && !rec)) return TP_ERR_NULL;
+        if (!aligned(grad_out, 8) || !aligned(rot, 4) || (rec && !aligned(rec, 8)) ||
+            (shift && !aligned(shift, 4)))
+            return TP_ERR_VALUE;
+    }
+    if ((grad_rec && !aligned(grad_rec, 8)) || (grad_rot && !aligned(grad_rot, 4)) ||
+        (grad_shift && !aligned(grad_shift, 4)))
+        return TP_ERR_VALUE;
+    const tp::Geom g = make_geom(ndim, n_rec, Dv, n_rot, n_pose, shift, n_sh, Do, o);
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    const int k2 = ndim * ndim;
+    const size_t n_sh_rows = shift ? (size_t)n_sh : 1;
+    if (grad_rec && n_rec > 0 &&
+        cudaMemsetAsync(grad_rec, 0, (size_t)g.rec_elems * n_rec * 8, s) != cudaSuccess)
+        return TP_ERR_CUDA;
+    if (grad_rot && cudaMemsetAsync(grad_rot, 0, (size_t)n_rot * n_pose * k2 * 4, s) != cudaSuccess)
+        return TP_ERR_CUDA;
+    if (grad_shift && cudaMemsetAsync(grad_shift, 0, n_sh_rows * n_pose * 2 * 4, s) != cudaSuccess)
+        return TP_ERR_CUDA;
+    if (n_items == 0 || (!grad_rec && !want_grad)) return TP_OK;
+    const int sms = sm_count();
+    use_ws = use_ws && want_grad;  // only the pose-gradient gather reads the grouped copy
+    cudaError_t e = cudaSuccess;
+    if (use_ws) e = tp::launch_expand_groups(o.interp, g, rec, workspace, sms, s);
+    if (e == cudaSuccess)
+        e = tp::launch_backward(ndim, o.interp, g, rec, rot, shift, grad_out, grad_rec, grad_rot,
+                                grad_shift, sms, s, use_ws ? workspace : nullptr, fused);
+    return e == cudaSuccess ? TP_OK : TP_ERR_CUDA;
+}
+
 }  // namespace
 
 extern "C" {
@@ -243,51 +291,24 @@ tp_status tp_project_backward(int ndim, const void* rec, int n_rec, int Dv, cons
                                   Do, grad_rec, grad_rot, grad_shift, nullptr, 0, opts, stream);
 }
 
+tp_status tp_project_backward_fused(int ndim, const void* rec, int n_rec, int Dv, const float* rot,
+                                    int n_rot, int n_pose, const float* shift, int n_sh,
+                                    const void* grad_out, int Do, void* grad_rec, float* grad_rot,
+                                    float* grad_shift, const tp_opts* opts, void* stream)
+{
+    return project_backward_impl(ndim, rec, n_rec, Dv, rot, n_rot, n_pose, shift, n_sh, grad_out,
+                                 Do, grad_rec, grad_rot, grad_shift, nullptr, 0, opts, stream, true);
+}
+
 tp_status tp_project_backward_ws(int ndim, const void* rec, int n_rec, int Dv, const float* rot,
                                  int n_rot, int n_pose, const float* shift, int n_sh,
                                  const void* grad_out, int Do, void* grad_rec, float* grad_rot,
                                  float* grad_shift, void* workspace, size_t workspace_bytes,
                                  const tp_opts* opts, void* stream)
 {
-    Opts o;
-    tp_status st = read_opts(opts, o);
-    if (st != TP_OK) return st;
-    st = check_common(ndim, n_rec, Dv, Do, n_rot, n_pose, shift, n_sh);
-    if (st != TP_OK) return st;
-    bool use_ws = false;
-    st = check_workspace(ndim, n_rec, Dv, o.interp, workspace, workspace_bytes, use_ws);
-    if (st != TP_OK) return st;
-    const long long n_items = (long long)n_rec * n_pose;
-    const bool want_grad = grad_rot || (grad_shift && shift);
-    if (n_items > 0 && (grad_rec || want_grad)) {
-        if (!grad_out || !rot || (want_grad && !rec)) return TP_ERR_NULL;
-        if (!aligned(grad_out, 8) || !aligned(rot, 4) || (rec && !aligned(rec, 8)) ||
-            (shift && !aligned(shift, 4)))
-            return TP_ERR_VALUE;
-    }
-    if ((grad_rec && !aligned(grad_rec, 8)) || (grad_rot && !aligned(grad_rot, 4)) ||
-        (grad_shift && !aligned(grad_shift, 4)))
-        return TP_ERR_VALUE;
-    const tp::Geom g = make_geom(ndim, n_rec, Dv, n_rot, n_pose, shift, n_sh, Do, o);
-    cudaStream_t s = static_cast<cudaStream_t>(stream);
-    const int k2 = ndim * ndim;
-    const size_t n_sh_rows = shift ? (size_t)n_sh : 1;
-    if (grad_rec && n_rec > 0 &&
-        cudaMemsetAsync(grad_rec, 0, (size_t)g.rec_elems * n_rec * 8, s) != cudaSuccess)
-        return TP_ERR_CUDA;
-    if (grad_rot && cudaMemsetAsync(grad_rot, 0, (size_t)n_rot * n_pose * k2 * 4, s) != cudaSuccess)
-        return TP_ERR_CUDA;
-    if (grad_shift && cudaMemsetAsync(grad_shift, 0, n_sh_rows * n_pose * 2 * 4, s) != cudaSuccess)
-        return TP_ERR_CUDA;
-    if (n_items == 0 || (!grad_rec && !want_grad)) return TP_OK;
-    const int sms = sm_count();
-    use_ws = use_ws && want_grad;  // only the pose-gradient gather reads the grouped copy
-    cudaError_t e = cudaSuccess;
-    if (use_ws) e = tp::launch_expand_groups(o.interp, g, rec, workspace, sms, s);
-    if (e == cudaSuccess)
-        e = tp::launch_backward(ndim, o.interp, g, rec, rot, shift, grad_out, grad_rec, grad_rot,
-                                grad_shift, sms, s, use_ws ? workspace : nullptr);
-    return e == cudaSuccess ? TP_OK : TP_ERR_CUDA;
+    return project_backward_impl(ndim, rec, n_rec, Dv, rot, n_rot, n_pose, shift, n_sh, grad_out,
+                                 Do, grad_rec, grad_rot, grad_shift, workspace, workspace_bytes,
+                                 opts, stream, false);
 }
 
 tp_status tp_backproject_backward(int ndim, const void* proj, const float* weights, int n_rec,

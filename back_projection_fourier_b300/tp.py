@@ -51,6 +51,7 @@ def _load() -> ctypes.CDLL:
     L.tp_backproject_2d_to_3d.argtypes = [P, P, I, I, P, I, I, P, I, P, P, I, I, O, P]
     L.tp_backproject_2d_to_2d.argtypes = [P, P, I, I, P, I, I, P, I, P, P, I, I, O, P]
     L.tp_project_backward.argtypes = [I, P, I, I, P, I, I, P, I, P, I, P, P, P, O, P]
+    L.tp_project_backward_fused.argtypes = [I, P, I, I, P, I, I, P, I, P, I, P, P, P, O, P]
     L.tp_backproject_backward.argtypes = [I, P, P, I, I, P, I, I, P, I, P, P, I, P, P, P, P, O, P]
     Z = ctypes.c_size_t
     L.tp_workspace_size.argtypes = [I, I, I, O]
@@ -65,7 +66,8 @@ def _load() -> ctypes.CDLL:
     for f in (L.tp_project_3d_to_2d, L.tp_project_2d_to_2d, L.tp_backproject_2d_to_3d,
               L.tp_backproject_2d_to_2d, L.tp_project_backward, L.tp_backproject_backward,
               L.tp_pad_volume, L.tp_crop_volume, L.tp_project_3d_to_2d_ws,
-              L.tp_project_backward_ws, L.tp_project_3d_to_2d_noalloc):
+              L.tp_project_backward_ws, L.tp_project_3d_to_2d_noalloc,
+              L.tp_project_backward_fused):
         f.restype = I
     return L
 
@@ -236,6 +238,16 @@ def tp_project_backward(ndim, rec, rot, shift, grad_out, grad_rec, grad_rot, gra
                                    _stream(stream)), "tp_project_backward")
 
 
+def tp_project_backward_fused(ndim, rec, rot, shift, grad_out, grad_rec, grad_rot, grad_shift,
+                              opts=None, stream=None):
+    n_rec, Dv, n_rot, n_pose, n_sh, Do = _backward_checks(ndim, rec, rot, shift, grad_out,
+                                                          grad_rec, grad_rot, grad_shift)
+    _call(_LIB.tp_project_backward_fused(int(ndim), _ptr(rec), n_rec, Dv, _ptr(rot), n_rot,
+                                         n_pose, _ptr(shift), n_sh, _ptr(grad_out), Do,
+                                         _ptr(grad_rec), _ptr(grad_rot), _ptr(grad_shift),
+                                         _opts(opts), _stream(stream)), "tp_project_backward_fused")
+
+
 def tp_backproject_backward(ndim, proj, weights, rot, shift, grad_vol, grad_wvol, grad_proj,
                             grad_weights, grad_rot, grad_shift, opts=None, stream=None):
     n_rot, n_pose, n_sh, items = _rs(rot, shift, ndim)
@@ -347,15 +359,17 @@ def backproject(proj, rot, shift=None, weights=None, Dv=None, want_weights=True,
 
 
 def project_backward(rec, rot, grad_out, shift=None, want_rec=True, want_rot=True,
-                     want_shift=True, opts=None, stream=None):
-    """Fused backward: (grad_rec, grad_rot, grad_shift), each None when not wanted."""
+                     want_shift=True, opts=None, stream=None, fused=False):
+    """Backward of the projection in one call: (grad_rec, grad_rot, grad_shift), each None when
+    not wanted.  fused=True takes tp_project_backward_fused (one kernel pass where it applies)."""
     ndim = rec.dim() - 1
     g_rec = torch.empty_like(rec) if want_rec else None
     g_rot = torch.empty_like(rot) if want_rot else None
     n_sh = shift.shape[0] if shift is not None else 1
     g_sh = torch.empty((n_sh, rot.shape[1], 2), dtype=torch.float32, device=rec.device) \
         if want_shift else None
-    tp_project_backward(ndim, rec, rot, shift, grad_out, g_rec, g_rot, g_sh, opts, stream)
+    (tp_project_backward_fused if fused else tp_project_backward)(
+        ndim, rec, rot, shift, grad_out, g_rec, g_rot, g_sh, opts, stream)
     return g_rec, g_rot, g_sh
 
 

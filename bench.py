@@ -50,6 +50,9 @@ def parse():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD)
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--fused-backward", action="store_true",
+                    help="the step's backward as one kernel pass (tp_project_backward_fused; "
+                         "no e2e leg)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-sample", type=int, default=16384, help="poses in the oracle sample")
     ap.add_argument("--batch", type=int, default=None,
@@ -246,14 +249,15 @@ def l2_policy(wl) -> tuple[bool, str]:
                    f"per kernel); no flush")
 
 
-def workload_config(wl, l2: str) -> dict:
+def workload_config(wl, l2: str, fused: bool = False) -> dict:
     world = dist_env()[0]
     par = "dp1" if world == 1 else f"dp{world} (pose shards of {wl.B} per rank, one volume all-reduce)"
+    step = ("forward + one-pass backward (tp_project_backward_fused)" if fused else
+            "forward + backward (volume, rotation and shift gradients)")
     return {"workload": wl.name, "D": wl.D, "batch": wl.B, "n_rec": wl.n_rec, "parallelism": par,
             "interp": "cubic" if wl.interp else "linear",
             "cutoff": wl.rc, "shift_amp": wl.extra["shift_amp"],
-            "layout": "centered" if wl.layout else "fftw", "step": "forward + fused backward",
-            "l2": l2}
+            "layout": "centered" if wl.layout else "fftw", "step": step, "l2": l2}
 
 
 def hbm_bytes(wl):
@@ -268,7 +272,9 @@ def hbm_bytes(wl):
     vol = wl.rec.nbytes
     return {"forward": wl.B * (img + pose) + vol,
             "grad_pose": wl.B * (img + 2 * pose) + vol,
-            "grad_volume": wl.B * (img + pose) + vol}
+            "grad_volume": wl.B * (img + pose) + vol,
+            # one pass: the upstream gradient read once, the volume read, its gradient written
+            "backward_fused": wl.B * (img + 2 * pose) + 2 * vol}
 
 
 def measure_peaks(dev) -> dict | None:
@@ -296,18 +302,24 @@ def onchip_work(wl) -> dict:
     scatter = {"taps": taps, "rmw": taps, "flop": 4 * taps}
     # the insertion with weights adds a float read-modify-write per tap: half the shared
     # bytes of a float2 one, counted as half of one
+    insertion = {"taps": taps, "rmw": taps * 3 // 2, "flop": 6 * taps}
+    if wl.ndim == 3 and not wl.interp:
+        # the linear 3D scatter adds each tap with shared float atomics (two pixels of a
+        # warp may share a voxel): 2 per tap, 3 with the weights
+        scatter = dict(scatter, smem_red=2 * taps)
+        insertion = dict(insertion, smem_red=3 * taps)
     return {"forward": gather, "grad_pose": dict(gather, flop=8 * taps + 16 * rows),
-            "grad_volume": scatter, "grad_image": scatter,
-            "insertion": {"taps": taps, "rmw": taps * 3 // 2, "flop": 6 * taps}}
+            "grad_volume": scatter, "grad_image": scatter, "insertion": insertion}
 
 
 def relevant_roofline(wl, kms, hbm, hbm_peak, pk, sm_mhz) -> dict | None:
     """Per kernel: T_roof = max(HBM bytes / HBM peak, tap bytes / L1 load peak, flops / FP32
     peak, scatter read-modify-writes / shared-memory read-modify-write peak), every peak
     measured (HBM by the driver's copy; the rest by the microbenchmarks of this run);
-    frac = T_roof / measured kernel time.  `row_gather_frac` sets the gathers' tap rows
-    against the measured rate of random 32-byte L1 loads (the gathers' access pattern) as
-    context."""
+    frac = T_roof / measured kernel time.  As context, `row_gather_frac` sets the gathers' tap
+    rows against the measured rate of random 32-byte L1 loads (the gathers' access pattern),
+    and `smem_red_frac` the linear 3D scatter's shared float atomics against the measured
+    shared atomic rate (the operation that kernel issues)."""
     if not pk:
         return None
     work = onchip_work(wl)
@@ -327,6 +339,8 @@ def relevant_roofline(wl, kms, hbm, hbm_peak, pk, sm_mhz) -> dict | None:
                "frac": 1e3 * t[bound] / ms, "t_ms": {u: 1e3 * v for u, v in t.items()}}
         if "rows" in w:
             ent["row_gather_frac"] = w["rows"] / pk["l1_gather32"]["ops_per_s"] / (ms * 1e-3)
+        if "smem_red" in w:
+            ent["smem_red_frac"] = w["smem_red"] / pk["smem_red"]["ops_per_s"] / (ms * 1e-3)
         out[k] = ent
     sms = pk.get("sms")
     if sm_mhz and sms:
@@ -407,9 +421,10 @@ def run_ours(args, wl):
     # (one short kernel) before its gather
     WS = tp.workspace_for(V, op)
 
-    # The fused backward is issued as two C-ABI calls (pose gradients, then the volume
-    # gradient): the same outputs as one call, but each call is one gather or one scatter,
-    # so CUDA events give every kernel's own duration.  The step is the package's
+    # The backward is issued as two C-ABI calls (pose gradients, then the volume gradient):
+    # the same outputs as one tp_project_backward call, but each call is one gather or one
+    # scatter, so CUDA events give every kernel's own duration.  With --fused-backward it is
+    # one tp_project_backward_fused call (one kernel).  The step is the package's
     # data-parallel step: on N ranks each holds its own pose shard and the volume gradient
     # is summed with one all-reduce (a no-op on one rank).
     cur_ev = [None]
@@ -425,9 +440,13 @@ def run_ours(args, wl):
         return Y
 
     def backward(V_, R_, S_, G_):
-        tp.tp_project_backward_ws(3, V_, R_, S_, G_, None, gR, gS, WS, op, stream)
-        mark(2)
-        tp.tp_project_backward(3, V_, R_, S_, G_, gV, None, None, op, stream)
+        if args.fused_backward:
+            mark(2)
+            tp.tp_project_backward_fused(3, V_, R_, S_, G_, gV, gR, gS, op, stream)
+        else:
+            tp.tp_project_backward_ws(3, V_, R_, S_, G_, None, gR, gS, WS, op, stream)
+            mark(2)
+            tp.tp_project_backward(3, V_, R_, S_, G_, gV, None, None, op, stream)
         mark(3)
         return gV, gR, gS
 
@@ -472,9 +491,12 @@ def run_ours(args, wl):
         t = torch.tensor([ms], device=dev)
         dist.all_reduce(t, op=dist.ReduceOp.MAX)
         ms = float(t.item())
-    kms = {"forward": statistics.mean(e[0].elapsed_time(e[1]) for e in evs),
-           "grad_pose": statistics.mean(e[1].elapsed_time(e[2]) for e in evs),
-           "grad_volume": statistics.mean(e[2].elapsed_time(e[3]) for e in evs)}
+    kms = {"forward": statistics.mean(e[0].elapsed_time(e[1]) for e in evs)}
+    if args.fused_backward:
+        kms["backward_fused"] = statistics.mean(e[2].elapsed_time(e[3]) for e in evs)
+    else:
+        kms["grad_pose"] = statistics.mean(e[1].elapsed_time(e[2]) for e in evs)
+        kms["grad_volume"] = statistics.mean(e[2].elapsed_time(e[3]) for e in evs)
     # with an L2 flush between steps the step time is the sum of the calls' own events
     ms_step = ms / args.steps if flush is None else sum(kms.values())
     if flush is not None and world > 1:
@@ -485,7 +507,7 @@ def run_ours(args, wl):
 
     # e2e: host (pinned) inputs -> device -> forward + backward -> host outputs, every step
     e2e = None
-    if not args.no_e2e:
+    if not args.no_e2e and not args.fused_backward:
         hV, hR, hG = V.cpu().pin_memory(), R.cpu().pin_memory(), G.cpu().pin_memory()
         hS = S.cpu().pin_memory() if S is not None else None
 
@@ -651,8 +673,9 @@ def run_ours(args, wl):
             "ms_per_step_median": statistics.median(e[0].elapsed_time(e[3]) for e in evs),
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
             "data": "synthetic (seeded rfft of N(0,1) volume, uniform SO(3), CN(0,1) upstream grad)",
-            "config": workload_config(wl, l2_note),
-            "gpu_launches": (3 + 2 * (WS is not None)) * args.steps,
+            "config": workload_config(wl, l2_note, args.fused_backward),
+            "gpu_launches": ((2 + (WS is not None)) if args.fused_backward else
+                             (3 + 2 * (WS is not None))) * args.steps,
             "kernel_ms": kms,
             "roofline": roofline, "roofline_relevant": relevant, "peaks_measured": onchip_peaks,
             "cpu_baseline": cpu, "e2e": e2e, "clocks": clocks,

@@ -138,6 +138,21 @@ tp_status tp_project_backward(int ndim, const void* rec, int n_rec, int Dv, cons
                               const void* grad_out, int Do, void* grad_rec, float* grad_rot,
                               float* grad_shift, const tp_opts* opts, void* stream);
 
+/* tp_project_backward in one kernel pass.  The pages' CUDA backend computes each operation in
+ * a single kernel call without stored intermediates (nl page, Belangrijkste Bijdragen, item 1;
+ * Methodologie, Differentiatie bullet).  For ndim = 3 with cubic interpolation, when grad_rec
+ * and grad_rot or grad_shift are requested, one kernel reads grad_out once and emits the
+ * volume, rotation and shift gradients together: the lanes of the volume-gradient scatter also
+ * read the volume at their taps and sum the pose terms.  In every other case the call is
+ * tp_project_backward.  Arguments, layouts, results and errors as tp_project_backward; the
+ * results agree with it to rounding (the summation order differs).  On B300 the one-pass
+ * kernel is slower than tp_project_backward's two kernels: the extra per-tap work goes to a
+ * kernel that is already bound by instruction issue and by the shared-memory pipe. */
+tp_status tp_project_backward_fused(int ndim, const void* rec, int n_rec, int Dv, const float* rot,
+                                    int n_rot, int n_pose, const float* shift, int n_sh,
+                                    const void* grad_out, int Do, void* grad_rec, float* grad_rot,
+                                    float* grad_shift, const tp_opts* opts, void* stream);
+
 /* Optional workspace of the 3D gathers.  tp_project_3d_to_2d_ws and tp_project_backward_ws
  * are tp_project_3d_to_2d and tp_project_backward with a caller-owned device workspace; the
  * results are the same (the same taps, weights and summation order).  The call first writes

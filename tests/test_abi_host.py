@@ -23,7 +23,7 @@ def test_header_symbols_are_exported():
                           "tp_backproject_2d_to_2d", "tp_project_backward", "tp_backproject_backward",
                           "tp_pad_volume", "tp_crop_volume", "tp_status_string",
                           "tp_workspace_size", "tp_project_3d_to_2d_ws", "tp_project_backward_ws",
-                          "tp_project_3d_to_2d_noalloc"}
+                          "tp_project_3d_to_2d_noalloc", "tp_project_backward_fused"}
     for n in names:
         assert hasattr(L, n), n
     dyn = subprocess.run(["nm", "-D", "--defined-only", str(tp.LIB_PATH)], capture_output=True,
@@ -85,13 +85,16 @@ def test_backproject_argument_errors():
     assert bp2(FAKE, None, 2, 8, FAKE, 3, 1, None, 1, FAKE, None, 8, 0, opts(), None) == 2
 
 
-def test_backward_argument_errors():
-    bw = L.tp_project_backward
+@pytest.mark.parametrize("entry", ["tp_project_backward", "tp_project_backward_fused"])
+def test_backward_argument_errors(entry):
+    bw = getattr(L, entry)
     assert bw(4, FAKE, 1, 8, FAKE, 1, 2, None, 1, FAKE, 8, FAKE, None, None, opts(), None) == 3
     assert bw(3, FAKE, 1, 8, FAKE, 1, 2, None, 1, None, 8, FAKE, None, None, opts(), None) == 1
     assert bw(3, None, 1, 8, FAKE, 1, 2, None, 1, FAKE, 8, None, FAKE, None, opts(), None) == 1
+    assert bw(3, None, 1, 8, FAKE, 1, 2, None, 1, FAKE, 8, FAKE, FAKE, None, opts(), None) == 1
     assert bw(3, FAKE, 1, 8, FAKE, 1, 2, None, 1, FAKE, 6, FAKE, None, None, opts(cutoff=math.inf), None) == 3
     assert bw(2, FAKE, 2, 8, FAKE, 1, 2, FAKE, 3, FAKE, 8, FAKE, None, None, opts(), None) == 2
+    assert bw(3, FAKE, 1, 8, FAKE, 1, 2, None, 1, FAKE, 8, MIS, FAKE, None, opts(), None) == 3
 
 
 def test_backproject_backward_argument_errors():
@@ -228,6 +231,8 @@ def test_binding_checks_every_shape_before_the_device():
             tp.tp_project_backward(3, *args)
         with pytest.raises(ValueError, match="must have shape"):
             tp.tp_project_backward_ws(3, *args, None)
+        with pytest.raises(ValueError, match="must have shape"):
+            tp.tp_project_backward_fused(3, *args)
 
 
 def test_binding_checks_insertion_and_padding_shapes():

@@ -62,3 +62,24 @@ def test_relevant_roofline_arithmetic():
     assert r["grad_volume"]["t_roof_ms"] == pytest.approx(1e3 * taps / 2e12)
     assert r["per_sm_per_clk"]["l1_load_B"] == pytest.approx(1e13 / (2000e6 * 148))
     assert bench.relevant_roofline(wl, kms, hbm, 6400.0, None, 2000.0) is None
+
+
+def test_shared_atomic_context_of_the_linear_insertion():
+    """The linear 3D scatter adds each of a pixel's 8 taps with shared float atomics: 3 per tap
+    with the weights (data re, im and weight).  Its context fraction sets those atomics
+    against the shared atomic rate; the bound stays the read-modify-write one (1.5 per tap).
+    The cubic tile scatter issues no shared atomics and has no such figure."""
+    wl = synth.make_workload("insert3d_d128_b16384", B=16, interp=synth.LINEAR, with_grad=False)
+    taps = 6490 * 16 * 8
+    pk = {"sms": 148, "l1_load": {"bytes_per_s": 1e13}, "l1_gather8": {"ops_per_s": 1e11},
+          "l1_gather32": {"ops_per_s": 2e11}, "smem_rmw": {"ops_per_s": 2e12},
+          "smem_rmw_random": {"ops_per_s": 1e12}, "smem_red": {"ops_per_s": 5e11},
+          "l2_red": {"ops_per_s": 2e11}, "fma": {"ops_per_s": 7e13}}
+    hbm = {"insertion": 1e6}
+    r = bench.relevant_roofline(wl, {"insertion": 2.0}, hbm, 6400.0, pk, 2000.0)
+    assert r["insertion"]["bound"] == "smem_rmw"
+    assert r["insertion"]["t_roof_ms"] == pytest.approx(1e3 * (taps * 3 // 2) / 2e12)
+    assert r["insertion"]["smem_red_frac"] == pytest.approx(3 * taps / 5e11 / 2e-3)
+    wc = synth.make_workload("insert3d_d128_b16384", B=16, interp=synth.CUBIC, with_grad=False)
+    rc = bench.relevant_roofline(wc, {"insertion": 2.0}, hbm, 6400.0, pk, 2000.0)
+    assert "smem_red_frac" not in rc["insertion"]

@@ -82,6 +82,31 @@ def test_backward(case):
         assert max_rel(host(g_sh), r_sh) <= TOL_BWD
 
 
+@pytest.mark.parametrize("case", CASES, ids=[str(c) for c in CASES])
+def test_backward_fused(case):
+    """tp_project_backward_fused: in 3D cubic one kernel pass emits the volume, rotation and
+    shift gradients (including the cases whose taps reach the x <= 0 planes, the rim, or
+    tiles too large for a box at o = 2); elsewhere it is the two-kernel call.  Either way the
+    oracle's gradients."""
+    ndim = case[0]
+    rec, rot, shift, grad, _, kw, op = make_case(case, seed=1)
+    r_rec, r_rot, r_sh = oracle.project_backward(ndim, rec, rot, grad, shift, **kw)
+    g_rec, g_rot, g_sh = tp.project_backward(dev(rec), dev(rot), dev(grad), dev(shift),
+                                             want_shift=shift is not None, opts=op, fused=True)
+    assert max_rel(host(g_rec), r_rec) <= TOL_BWD
+    assert max_rel(host(g_rot), r_rot) <= TOL_BWD
+    if ndim == 3:
+        assert np.all(host(g_rot)[..., 2] == 0)
+    if shift is not None:
+        assert max_rel(host(g_sh), r_sh) <= TOL_BWD
+        # the shift gradient alone beside the volume gradient (still one pass)
+        g_rec2, g_none, g_sh2 = tp.project_backward(dev(rec), dev(rot), dev(grad), dev(shift),
+                                                    want_rot=False, opts=op, fused=True)
+        assert g_none is None
+        assert max_rel(host(g_rec2), r_rec) <= TOL_BWD
+        assert max_rel(host(g_sh2), r_sh) <= TOL_BWD
+
+
 @pytest.mark.parametrize("case", PARTIAL, ids=[str(c) for c in PARTIAL])
 def test_backward_partial_outputs(case):
     """Each gradient output may be skipped (NULL); the others are unchanged."""

@@ -168,6 +168,34 @@ def test_fwdbwd3d_d256_cubic_full_sampled():
     _fwdbwd3d_sampled("fwdbwd3d_d256_cubic_b50000", n_pix=4000, n_poses=24, n_sub=256)
 
 
+def test_fwdbwd3d_d128_cubic_fused_backward():
+    """tp_project_backward_fused (one kernel pass) on the headline workload: the whole batch
+    against the two-kernel call, the pose gradients of sampled poses and the volume gradient of
+    a 512-pose sub-batch (every voxel) against the oracle."""
+    wl = synth.make_workload("fwdbwd3d_d128_cubic_b16384")
+    V, R, S, G = dev(wl.rec), dev(wl.rot), dev(wl.shift), dev(wl.grad)
+    op = wl_opts(wl)
+    kw = oracle_kw(wl)
+    fused = tp.project_backward(V, R, G, S, opts=op, fused=True)
+    two = tp.project_backward(V, R, G, S, opts=op)
+    for a, b in zip(fused, two):
+        assert max_rel(host(a), host(b)) <= TOL_BWD
+    rng = np.random.default_rng(12)
+    poses = np.sort(rng.choice(wl.n_pose, 48, replace=False))
+    _, r_rot, r_sh = oracle.project_backward(3, wl.rec, sub(wl.rot, poses), sub(wl.grad, poses),
+                                             sub(wl.shift, poses), want_rec=False, **kw)
+    tpo = torch.from_numpy(poses).cuda()
+    assert max_rel(host(fused[1][:, tpo]), r_rot) <= TOL_BWD
+    assert max_rel(host(fused[2][:, tpo]), r_sh) <= TOL_BWD
+    n_sub = 512
+    sl = lambda t: t[:, :n_sub].contiguous()  # noqa: E731
+    g_sub, _, _ = tp.project_backward(V, sl(R), sl(G), sl(S), opts=op, fused=True)
+    idx = np.arange(n_sub)
+    r_rec, _, _ = oracle.project_backward(3, wl.rec, sub(wl.rot, idx), sub(wl.grad, idx),
+                                          sub(wl.shift, idx), want_rot=False, want_shift=False, **kw)
+    assert max_rel(host(g_sub), r_rec) <= TOL_BWD
+
+
 def test_chunked_volume_gradient_equals_the_backward():
     """The pipelined end-to-end step sums each pose chunk's volume gradient with the insertion
     call (accumulate = 1): the same transpose as the backward's volume gradient."""
