@@ -1074,7 +1074,11 @@ scatter_tile_kernel(const float2* __restrict__ proj, const float* __restrict__ w
                     // effective value: conj(g') on the mirrored pass (weights are real)
                     rf[TR::GX] = gp.x;
                     rf[TR::GY] = sg * gp.y;
-                    const int base = ((fz + FIRST - z0) * NY + (fy + FIRST - y0)) * PITCH + (fx + FIRST - x0);
+                    // the box offset of the pixel's first tap (below CAP); 0 without a box, so
+                    // that the per-tap flag ~base below is negative whatever the extents (the
+                    // product would overflow for extents near the 2^23 clamp)
+                    const int base = boxed ? ((fz + FIRST - z0) * NY + (fy + FIRST - y0)) * PITCH + (fx + FIRST - x0)
+                                           : 0;
                     // (POSE: taps past x = Dv/2 also take the per-tap path, where the volume
                     // reads follow the exact rule)
                     ri[TR::BASE] = (fx + FIRST <= 0 || !boxed || (POSE && fx + FIRST + NT - 1 > g.halfv))

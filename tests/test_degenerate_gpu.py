@@ -81,3 +81,33 @@ def test_degenerate_poses_2d():
     rr, rg, _ = oracle.project_backward(2, img[ok], rot[ok], grad[ok], shift[ok], interp=1, layout=1)
     assert max_rel(host(g_rec)[ok], rr) <= TOL_BWD
     assert max_rel(host(g_rot)[ok], rg) <= TOL_BWD
+
+
+@pytest.mark.parametrize("interp", [0, 1])
+def test_huge_finite_rotation_with_data(interp):
+    """A finite rotation scaled by 1e7 sends every pixel but (0, 0) far outside the band, where
+    the kernels clamp the coordinate to +-2^23: tiles of the scatter then span extents near 2^24
+    and take the per-tap path.  With non-zero upstream data on that pose the volume gradient
+    and the insertion still match the oracle (fp64, no clamp needed at 1e7), which counts only
+    pixel (0, 0) of it."""
+    rng = np.random.default_rng(41 + interp)
+    D = 24
+    op = opts(interp)
+    kw = dict(interp=interp, layout=1)
+    rot = rotations(rng, 4, 3).astype(np.float32)
+    rot[1] *= 1e7
+    rot = rot[None]
+    shift = rng.uniform(-4, 4, (1, 4, 2)).astype(np.float32)
+    vol = crandn32(rng, (1, D, D, D // 2 + 1))
+    grad = crandn32(rng, (1, 4, D, D // 2 + 1))
+    w = rng.uniform(0.1, 1, grad.shape).astype(np.float32)
+    V, R, S, G = dev(vol), dev(rot), dev(shift), dev(grad)
+    g_rec = torch.empty_like(V)
+    tp.tp_project_backward(3, V, R, S, G, g_rec, None, None, op)
+    vol_bp, w_bp = tp.backproject(G, R, S, dev(w), opts=op)
+    r_rec, _, _ = oracle.project_backward(3, vol, rot, grad, shift, want_rot=False,
+                                          want_shift=False, **kw)
+    assert max_rel(host(g_rec), r_rec) <= TOL_BWD
+    r_vol, r_w = oracle.backproject(3, grad, rot, weights=w, shift=shift, **kw)
+    assert max_rel(host(vol_bp), r_vol) <= TOL_BWD
+    assert max_rel(host(w_bp), r_w) <= TOL_BWD

@@ -107,6 +107,23 @@ def test_backward_fused(case):
         assert max_rel(host(g_sh2), r_sh) <= TOL_BWD
 
 
+@pytest.mark.parametrize("case", [c for c in CASES if c[0] == 3 and c[1] == 1][:4],
+                         ids=[str(c) for c in CASES if c[0] == 3 and c[1] == 1][:4])
+def test_backward_gradient_at_odd_8_byte_offset(case):
+    """The volume gradient may start at any 8-byte boundary (the C ABI asks for 8): a buffer at
+    an odd multiple of 8 bytes gives the oracle's result like an aligned one."""
+    ndim = case[0]
+    rec, rot, shift, grad, _, kw, op = make_case(case, seed=6)
+    r_rec, _, _ = oracle.project_backward(ndim, rec, rot, grad, shift, want_rot=False,
+                                          want_shift=False, **kw)
+    V = dev(rec)
+    buf = torch.empty(V.numel() + 1, dtype=V.dtype, device="cuda")
+    g_rec = buf[1:].view(V.shape)
+    assert g_rec.data_ptr() % 16 == 8
+    tp.tp_project_backward(ndim, V, dev(rot), dev(shift), dev(grad), g_rec, None, None, op)
+    assert max_rel(host(g_rec), r_rec) <= TOL_BWD
+
+
 @pytest.mark.parametrize("case", PARTIAL, ids=[str(c) for c in PARTIAL])
 def test_backward_partial_outputs(case):
     """Each gradient output may be skipped (NULL); the others are unchanged."""
