@@ -1312,6 +1312,242 @@ scatter_tile_kernel(const float2* __restrict__ proj, const float* __restrict__ w
     }
 }
 
+// Cubic 2D insertion with weights (data and weight images together).  A half-warp takes a
+// 4 x 4 pixel tile with its own shared-memory box over the tile's tap footprint, so a warp
+// adds two pixels at a time, one per half-warp, with plain read-modify-writes: the 16 lanes
+// of a half-warp sit on the 16 taps of its pixel (distinct voxels), and __syncwarp orders
+// successive pixels.  Box rows have a pitch of 12 voxels, so a pixel's 4 tap rows fall in 4
+// distinct groups of 8 banks.  As in the 3D tile scatter, pixels with c_x < 0 go in a
+// second pass in the effective frame (c' = -c, conjugate value); pixels whose taps reach
+// x <= 0 take the exact per-tap rule (mirrored taps by global atomics), tiles whose box
+// would overflow (o > 1) add every tap by atomics, and the box is added to the image with
+// one vector reduction per touched voxel.
+constexpr int kTile2Pitch = 12;
+constexpr int kTile2Rows = 10;  // a 4 x 4 tile at o = 1 spans at most 9 rows
+constexpr int kTile2Threads = 256;
+
+// Record of one pixel: gx gy wt base (one 16-byte load) | wx[4] | wy[4] | fx fy.  base < 0
+// flags the per-tap path and holds ~base.
+struct Tile2Rec {
+    enum : int { GX = 0, GY = 1, WT = 2, BASE = 3, WX = 4, WY = 8, FX = 12, FY = 13, STRIDE = 16 };
+};
+
+template <bool DATA, bool WTS>
+__global__ void __launch_bounds__(kTile2Threads) scatter_tile2d_kernel(
+    const float2* __restrict__ proj, const float* __restrict__ wts,
+    const float* __restrict__ rot, const float* __restrict__ shift,
+    float2* __restrict__ vout, float* __restrict__ wout, Geom g, int splits, long long n_work)
+{
+    using TR = Tile2Rec;
+    constexpr int NT = 4, FIRST = -1;
+    constexpr int PITCH = kTile2Pitch, ROWS = kTile2Rows, CAP = PITCH * ROWS;
+    constexpr int NWARP = kTile2Threads / 32;
+    constexpr unsigned kFull = 0xffffffffu;
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const int h = lane >> 4, l = lane & 15;  // half-warp, lane within it
+    const int hw = warp * 2 + h;             // half-warp of the CTA
+    extern __shared__ __align__(16) unsigned char sm_raw[];
+    // per half-warp: acc[CAP] float2 | wacc[CAP] float | records [16][STRIDE]
+    float2* acc = reinterpret_cast<float2*>(sm_raw) + hw * (DATA ? CAP : 0);
+    float* wbase = reinterpret_cast<float*>(reinterpret_cast<float2*>(sm_raw) + 2 * NWARP * (DATA ? CAP : 0));
+    float* wacc = wbase + hw * (WTS ? CAP : 0);
+    float* recf = wbase + 2 * NWARP * (WTS ? CAP : 0) + hw * kTilePix * TR::STRIDE;
+    int* reci = reinterpret_cast<int*>(recf);
+
+    for (int e = l; e < CAP; e += 16) {
+        if (DATA) acc[e] = make_float2(0.f, 0.f);
+        if (WTS) wacc[e] = 0.f;
+    }
+    // this lane's tap: row tb, column tk of the pixel's 4 x 4 taps
+    const int tb = l >> 2, tk = l & 3;
+    const int toff = tb * PITCH + tk;
+    const int tiles_x = (g.Ho + 3) / 4, tiles_y = (g.Do + 3) / 4;
+    const int ntiles = tiles_x * tiles_y;
+
+    for (long long w = blockIdx.x; w < n_work; w += gridDim.x) {
+        const ItemRange ir = item_of(g, w, splits);
+        float Rs[4];
+        {
+            const long long ri = (long long)(g.rot_shared ? 0 : ir.r) * g.n_pose + ir.p;
+#pragma unroll
+            for (int k = 0; k < 4; ++k) Rs[k] = g.o * __ldg(rot + ri * 4 + k);
+        }
+        float2 sh = make_float2(0.f, 0.f);
+        if (g.has_shift) {
+            const long long si = (long long)(g.sh_shared ? 0 : ir.r) * g.n_pose + ir.p;
+            sh = make_float2(__ldg(shift + si * 2), __ldg(shift + si * 2 + 1));
+        }
+        const float2* py = DATA ? proj + ir.item * g.img_elems : nullptr;
+        const float* pw = (WTS && wts) ? wts + ir.item * g.img_elems : nullptr;  // NULL: weight 1
+        float2* G = DATA ? vout + (long long)ir.r * g.rec_elems : nullptr;
+        float* Wt = WTS ? wout + (long long)ir.r * g.rec_elems : nullptr;
+
+        // tiles in pairs: half-warp h of the warp takes tile t2 + h
+        for (int t2 = (ir.part * NWARP + warp) * 2; t2 < ntiles; t2 += splits * NWARP * 2) {
+            const int tile = t2 + h;
+            const bool tvalid = tile < ntiles;
+            const int ti = tvalid ? tile / tiles_x : 0, tj = tvalid ? tile - ti * tiles_x : 0;
+            const int prow = 4 * ti + (l >> 2), pkx = 4 * tj + (l & 3);
+            bool kept = false;
+            int ky = 0;
+            float cx = 0.f, cy = 0.f;
+            if (tvalid && prow < g.Do && pkx < g.Ho) {
+                ky = row_freq(prow, g.Do, g.halfo, g.centered);
+                kept = pkx * pkx + ky * ky <= g.rc2;
+                const float fkx = (float)pkx, fky = (float)ky;
+                cx = fmaf(Rs[0], fkx, Rs[1] * fky);
+                cy = fmaf(Rs[2], fkx, Rs[3] * fky);
+            }
+            const unsigned kept_mask = __ballot_sync(kFull, kept);
+            if (!kept_mask) continue;
+            const unsigned neg_mask = __ballot_sync(kFull, kept && cx < 0.f);
+            float2 gp = make_float2(0.f, 0.f);
+            float wt = 1.f;
+            if (kept) {
+                if (DATA) {
+                    gp = __ldg(py + prow * g.Ho + pkx);
+                    if (g.has_shift)
+                        gp = cmul_conj(gp, shift_phase((float)pkx, (float)ky, sh.x, sh.y, g.Do_f, g.inv_Do));
+                }
+                if (WTS && pw) wt = __ldg(pw + prow * g.Ho + pkx);
+            }
+            for (int pass = 0; pass < 2; ++pass) {
+                const unsigned wmask = pass ? neg_mask : (kept_mask & ~neg_mask);
+                if (!wmask) continue;
+                const unsigned pmask = (wmask >> (16 * h)) & 0xffffu;  // this half's pixels
+                const bool mine = (pmask >> l) & 1u;
+                const float sg = pass ? -1.f : 1.f;
+                // effective coordinates, clamped like floor_frac
+                const float lim = 8388608.0f;
+                const float ex = fminf(fmaxf(sg * cx, -lim), lim);
+                const float ey = fminf(fmaxf(sg * cy, -lim), lim);
+                const float flx = floorf(ex), fly = floorf(ey);
+                const int fx = (int)flx, fy = (int)fly;
+                // box of this half's pass: reductions within the half-warp
+                const int big = 1 << 28;
+                int mnx = mine ? fx : big, mny = mine ? fy : big;
+                int mxx = mine ? fx : -big, mxy = mine ? fy : -big;
+#pragma unroll
+                for (int o = 8; o > 0; o >>= 1) {
+                    mnx = min(mnx, __shfl_xor_sync(kFull, mnx, o));
+                    mny = min(mny, __shfl_xor_sync(kFull, mny, o));
+                    mxx = max(mxx, __shfl_xor_sync(kFull, mxx, o));
+                    mxy = max(mxy, __shfl_xor_sync(kFull, mxy, o));
+                }
+                const int x0 = mnx + FIRST, y0 = mny + FIRST;
+                const int NX = mxx - mnx + NT, NY = mxy - mny + NT;
+                const bool boxed = pmask != 0 && NX <= PITCH && NY <= ROWS;
+                if (mine) {
+                    float wx_[NT], wy_[NT];
+                    weights<kCubic>(ex - flx, wx_);
+                    weights<kCubic>(ey - fly, wy_);
+                    float* rf = recf + l * TR::STRIDE;
+                    int* ri = reci + l * TR::STRIDE;
+                    *reinterpret_cast<float4*>(rf + TR::WX) = make_float4(wx_[0], wx_[1], wx_[2], wx_[3]);
+                    *reinterpret_cast<float4*>(rf + TR::WY) = make_float4(wy_[0], wy_[1], wy_[2], wy_[3]);
+                    // the box offset of the first tap; 0 without a box (the flag stays negative)
+                    const int base = boxed ? (fy + FIRST - y0) * PITCH + (fx + FIRST - x0) : 0;
+                    *reinterpret_cast<float4*>(rf) =
+                        make_float4(gp.x, sg * gp.y, wt, __int_as_float((fx + FIRST <= 0 || !boxed) ? ~base : base));
+                    ri[TR::FX] = fx;
+                    ri[TR::FY] = fy;
+                }
+                __syncwarp();
+                // both halves step together for as many pixels as the fuller one has
+                const int cnt = __popc(pmask);
+                const int cmax = max(cnt, __shfl_xor_sync(kFull, cnt, 16));
+                unsigned m = pmask;
+                for (int it = 0; it < cmax; ++it) {
+                    if (m) {
+                        const int j = __ffs(m) - 1;
+                        m &= m - 1;
+                        const float* rf = recf + j * TR::STRIDE;
+                        const int* ri = reci + j * TR::STRIDE;
+                        const float4 head = *reinterpret_cast<const float4*>(rf);
+                        const float2 gv = make_float2(head.x, head.y);
+                        const float wtv = head.z;
+                        const int rb = __float_as_int(head.w);
+                        const float w = rf[TR::WY + tb] * rf[TR::WX + tk];
+                        if (rb >= 0) {
+                            const int e = rb + toff;
+                            if (DATA) {
+                                float2 a = acc[e];
+                                a.x = fmaf(w, gv.x, a.x);
+                                a.y = fmaf(w, gv.y, a.y);
+                                acc[e] = a;
+                            }
+                            if (WTS) wacc[e] = fmaf(w, wtv, wacc[e]);
+                        } else {
+                            // taps on the x <= 0 column (exact per-tap rule), or no box
+                            const int base = ~rb;
+                            const int ux = ri[TR::FX] + FIRST + tk;
+                            const bool direct = ux >= 1 || (ux == 0 && pass == 0);
+                            if (direct && boxed) {
+                                const int e = base + toff;
+                                if (DATA) {
+                                    float2 a = acc[e];
+                                    a.x = fmaf(w, gv.x, a.x);
+                                    a.y = fmaf(w, gv.y, a.y);
+                                    acc[e] = a;
+                                }
+                                if (WTS) wacc[e] = fmaf(w, wtv, wacc[e]);
+                            } else {
+                                // target u (direct) or -u (mirrored, conjugate value)
+                                int vx = ux, vy = ri[TR::FY] + FIRST + tb;
+                                float vim = gv.y;
+                                if (!direct) {
+                                    vx = -vx;
+                                    vy = -vy;
+                                    vim = -vim;
+                                }
+                                const int iy = full_index(vy, g.Dv, g.halfv, g.centered);
+                                if (vx >= 0 && vx <= g.halfv && iy >= 0) {
+                                    const int off = iy * g.Hv + vx;
+                                    if (DATA) atomicAdd(G + off, make_float2(w * gv.x, w * vim));
+                                    if (WTS) atomicAdd(Wt + off, w * wtv);
+                                }
+                            }
+                        }
+                    }
+                    __syncwarp();
+                }
+                // add the half's box to the image (read and clear the non-zero entries)
+                if (boxed) {
+                    const int nused = NX * NY;
+                    const unsigned mx = (65536u + NX - 1) / NX;
+                    for (int e = l; e < nused; e += 16) {
+                        const int r = (int)(((unsigned)e * mx) >> 16);
+                        const int xi = e - r * NX;
+                        const int be = r * PITCH + xi;
+                        float2 a = make_float2(0.f, 0.f);
+                        float b = 0.f;
+                        bool hit = false;
+                        if (DATA) {
+                            a = acc[be];
+                            hit = a.x != 0.f || a.y != 0.f;
+                        }
+                        if (WTS) {
+                            b = wacc[be];
+                            hit = hit || b != 0.f;
+                        }
+                        if (hit) {
+                            const int iy = full_index(y0 + r, g.Dv, g.halfv, g.centered);
+                            const int ux = x0 + xi;
+                            if (iy >= 0 && ux >= 0 && ux <= g.halfv) {
+                                if (DATA && (a.x != 0.f || a.y != 0.f)) atomicAdd(G + iy * g.Hv + ux, a);
+                                if (WTS && b != 0.f) atomicAdd(Wt + iy * g.Hv + ux, b);
+                            }
+                            if (DATA) acc[be] = make_float2(0.f, 0.f);
+                            if (WTS) wacc[be] = 0.f;
+                        }
+                    }
+                }
+                __syncwarp();
+            }
+        }
+    }
+}
+
 // Lane-per-pixel back-projection for linear 3D.  With 8 taps per pixel, the tile scatter's
 // lanes-on-taps mapping keeps only 8 lanes busy and pays its per-pixel record and loop costs 4
 // times over.  Here a warp takes an 8 x 4 tile of kept pixels, one pixel per lane, with the
@@ -1791,6 +2027,26 @@ void launch_scatter_tile(const Geom& g, const float2* P, const float* weights, c
 }
 
 template <bool DATA, bool WTS>
+void launch_scatter_tile2d(const Geom& g, const float2* P, const float* weights, const float* rot,
+                           const float* shift, float2* VO, float* WO, int sms, cudaStream_t stream)
+{
+    constexpr size_t cap = (size_t)kTile2Pitch * kTile2Rows;
+    constexpr int nwarp = kTile2Threads / 32;
+    const size_t per_half = (DATA ? cap * 8 : 0) + (WTS ? cap * 4 : 0) +
+                            (size_t)kTilePix * Tile2Rec::STRIDE * 4;
+    const size_t smem = per_half * 2 * nwarp;
+    auto kern = scatter_tile2d_kernel<DATA, WTS>;
+    cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    const long long n_items = (long long)g.n_rec * g.n_pose;
+    const long long ntiles = (long long)((g.Ho + 3) / 4) * ((g.Do + 3) / 4);
+    const int splits = (int)item_splits(n_items, 3LL * sms, (ntiles + 2 * nwarp - 1) / (2 * nwarp));
+    const long long n_work = n_items * splits;
+    const long long cap_grid = 8LL * sms;
+    const unsigned grid = (unsigned)(n_work < cap_grid ? n_work : cap_grid);
+    kern<<<grid, kTile2Threads, smem, stream>>>(P, weights, rot, shift, VO, WO, g, splits, n_work);
+}
+
+template <bool DATA, bool WTS>
 void launch_scatter_lane(const Geom& g, const float2* P, const float* weights, const float* rot,
                          const float* shift, float2* VO, float* WO, int sms, cudaStream_t stream)
 {
@@ -1831,6 +2087,15 @@ void launch_backproject_t(const Geom& g, const float2* P, const float* weights, 
         else
             launch_scatter_tile<INTERP, false, true>(g, P, weights, rot, shift, VO, WO, sms, stream);
     } else {
+        // 2D cubic with weights: the half-warp tile scatter (14.1 -> 10.4 ms for 8 192 images at
+        // D = 256); the data alone ties with the owner-computes rows kernel (8.36 ms both),
+        // which writes every voxel once, without atomics, and so keeps it
+        if constexpr (INTERP == kCubic) {
+            if (VO && WO) {
+                launch_scatter_tile2d<true, true>(g, P, weights, rot, shift, VO, WO, sms, stream);
+                return;
+            }
+        }
         if (VO && WO)
             launch_scatter_rows<NDIM, INTERP, true, true>(g, P, weights, rot, shift, VO, WO, sms, stream);
         else if (VO)
