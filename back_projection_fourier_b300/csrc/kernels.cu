@@ -410,7 +410,11 @@ __global__ void __launch_bounds__(kPoseThreads, 4) grad_pose_kernel(
     int* rowstart = smem;
     int* qslots = smem + g.Do + 1;           // [kWarpQueue per warp]
     __shared__ int scratch[kPoseThreads / 32];
-    __shared__ float red[kPoseThreads / 32];
+    // per-warp sums of the item's terms, double-buffered by work-unit parity: one barrier per
+    // work unit orders the writes before the sums, and the next unit writes the other buffer
+    constexpr int NWP = kPoseThreads / 32;
+    __shared__ float red[2][NG][NWP];
+    int parity = 0;
     build_rowstart<kPoseThreads>(g, rowstart, scratch);
     const int lane = threadIdx.x & 31;
     WarpQueue q{qslots + (threadIdx.x >> 5) * kWarpQueue, 0};
@@ -480,15 +484,25 @@ __global__ void __launch_bounds__(kPoseThreads, 4) grad_pose_kernel(
         const float two_pi_over_Do = 6.283185307179586f * g.inv_Do;
 #pragma unroll
         for (int k = 0; k < NG; ++k) {
-            const float s = block_sum<kPoseThreads>(acc[k], red);
-            if (threadIdx.x == 0) {
-                if (k < 2 * NDIM) {
-                    if (grot) atomicAdd(grot + ri * NDIM * NDIM + (k / 2) * NDIM + (k % 2), g.o * s);
-                } else if (gsh && g.has_shift) {
-                    atomicAdd(gsh + si * 2 + (k - 2 * NDIM), two_pi_over_Do * s);
-                }
+            float v = acc[k];
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+            if (lane == 0) red[parity][k][threadIdx.x >> 5] = v;
+        }
+        __syncthreads();
+        // thread k < NG adds term k over the warps
+        if (threadIdx.x < NG) {
+            const int k = threadIdx.x;
+            float s = 0.f;
+#pragma unroll
+            for (int wi = 0; wi < NWP; ++wi) s += red[parity][k][wi];
+            if (k < 2 * NDIM) {
+                if (grot) atomicAdd(grot + ri * NDIM * NDIM + (k / 2) * NDIM + (k % 2), g.o * s);
+            } else if (gsh && g.has_shift) {
+                atomicAdd(gsh + si * 2 + (k - 2 * NDIM), two_pi_over_Do * s);
             }
         }
+        parity ^= 1;
     }
 }
 
