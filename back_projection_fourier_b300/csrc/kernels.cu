@@ -943,11 +943,12 @@ constexpr int kOutside = -(1 << 30);
 // let four CTAs fit in shared memory.
 constexpr int kTileThreadsPose = 192;
 
-// POSE: the fused backward.  Besides the volume gradient the kernel forms the rotation and
+// POSE: the one-pass backward.  Besides the volume gradient the kernel forms the rotation and
 // shift gradients: every lane reads the volume at its two taps of the pixel (effective frame,
 // the exact Friedel rule on the per-tap path), and accumulates, over the item's pixels, the
 // terms o q_b Re(conj(g') dv/dc_a) and (2 pi / Do) q_b Im(conj(g') v) of each tap; a warp
-// reduction and one atomic per term per warp finish the item.
+// reduction and one atomic per term per warp finish the item.  The launch bound asks for four
+// CTAs per SM only with POSE (80 registers); 0 leaves the other instances unconstrained.
 template <int INTERP, bool DATA, bool WTS, bool POSE = false>
 __global__ void __launch_bounds__(POSE ? kTileThreadsPose : kTileThreads, POSE ? 4 : 0)
 scatter_tile_kernel(const float2* __restrict__ proj, const float* __restrict__ wts,
