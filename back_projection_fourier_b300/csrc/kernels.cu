@@ -229,6 +229,35 @@ __device__ __forceinline__ bool eval_fast(const Geom& g, const float2* __restric
     return true;
 }
 
+// Separable shift twiddles of one item (2D gathers): tw[kx] = phase(kx, 0) for kx < Ho and
+// tw[Ho + row] = phase(0, ky(row)) for the Do rows, so that a pixel's phase is one complex
+// product of two table entries instead of a phase evaluation (each factor is computed with the
+// exact turn reduction of shift_phase).  Two buffers alternate by work unit; the barrier after
+// each build also orders the previous unit's reads of the other buffer before its next build.
+constexpr int kMaxTwiddleRows = 1024;  // tables of at most 2 x (513 + 1024) entries, 24.6 KB
+
+__host__ __device__ __forceinline__ bool use_twiddles(const Geom& g, int ndim)
+{
+    return ndim == 2 && g.Do <= kMaxTwiddleRows;
+}
+
+__device__ __forceinline__ float2* twiddle_table(int* after_queues)
+{
+    // 8-byte aligned start after the int tables
+    const uintptr_t a = (reinterpret_cast<uintptr_t>(after_queues) + 7) & ~(uintptr_t)7;
+    return reinterpret_cast<float2*>(a);
+}
+
+template <int BT>
+__device__ __forceinline__ void build_twiddles(const Geom& g, float sx, float sy, float2* tw)
+{
+    for (int k = threadIdx.x; k < g.Ho + g.Do; k += BT)
+        tw[k] = k < g.Ho ? shift_phase((float)k, 0.f, sx, sy, g.Do_f, g.inv_Do)
+                         : shift_phase(0.f, (float)row_freq(k - g.Ho, g.Do, g.halfo, g.centered), sx,
+                                       sy, g.Do_f, g.inv_Do);
+    __syncthreads();
+}
+
 // ------------------------------------------------------------------ forward ----
 
 template <int NDIM, int INTERP, int WIN>
@@ -252,12 +281,17 @@ __global__ void __launch_bounds__(NDIM == 3 ? kFwd3Threads : kThreads, 4) projec
     const int nkept = rowstart[g.Do];
     const int npix = (int)g.img_elems;
     const int chunk = kept_chunk<BT>(nkept, splits);
+    float2* const tw0 = twiddle_table(qslots + kWarpQueue * (BT / 32));  // 2D: [2][Ho + Do]
+    int unit = 0;
 
     // work unit = (item, part): part takes one chunk of the item's kept pixels
-    for (long long w = blockIdx.x; w < n_work; w += gridDim.x) {
+    for (long long w = blockIdx.x; w < n_work; w += gridDim.x, ++unit) {
         const ItemRange ir = item_of(g, w, splits);
         ItemParams<NDIM> ip;
         load_item<NDIM>(g, rot, shift, ir.r, ir.p, ip);
+        float2* const tw = tw0 + (unit & 1) * (g.Ho + g.Do);
+        const bool twid = use_twiddles(g, NDIM) && g.has_shift;
+        if (twid) build_twiddles<BT>(g, ip.sx, ip.sy, tw);
         const float2* V = rec + (long long)ir.r * g.rec_elems;
         const float2* VG =
             WIN == kGrouped ? grouped + (long long)ir.r * g.Dv * g.gplane * Taps<INTERP>::N : V;
@@ -269,9 +303,12 @@ __global__ void __launch_bounds__(NDIM == 3 ? kFwd3Threads : kThreads, 4) projec
             if (j >= rowstart[i + 1] - rowstart[i]) y[p] = make_float2(0.f, 0.f);
         }
         auto finish = [&](int row, int kx, float2 val) {
-            const int ky = row_freq(row, g.Do, g.halfo, g.centered);
-            if (g.has_shift)
+            if (twid) {
+                val = cmul(val, cmul(tw[kx], tw[g.Ho + row]));
+            } else if (g.has_shift) {
+                const int ky = row_freq(row, g.Do, g.halfo, g.centered);
                 val = cmul(val, shift_phase((float)kx, (float)ky, ip.sx, ip.sy, g.Do_f, g.inv_Do));
+            }
             y[row * g.Ho + kx] = val;
         };
         const int b0 = ir.part * chunk, b1 = min(nkept, b0 + chunk);
@@ -420,12 +457,17 @@ __global__ void __launch_bounds__(kPoseThreads, 4) grad_pose_kernel(
     WarpQueue q{qslots + (threadIdx.x >> 5) * kWarpQueue, 0};
     const int nkept = rowstart[g.Do];
     const int chunk = kept_chunk<kPoseThreads>(nkept, splits);
+    float2* const tw0 = twiddle_table(qslots + kWarpQueue * (kPoseThreads / 32));  // 2D
+    int unit = 0;
 
     // work unit = (item, part): part sums one chunk of the item's kept pixels
-    for (long long w = blockIdx.x; w < n_work; w += gridDim.x) {
+    for (long long w = blockIdx.x; w < n_work; w += gridDim.x, ++unit) {
         const ItemRange ir = item_of(g, w, splits);
         ItemParams<NDIM> ip;
         load_item<NDIM>(g, rot, shift, ir.r, ir.p, ip);
+        float2* const tw = tw0 + (unit & 1) * (g.Ho + g.Do);
+        const bool twid = use_twiddles(g, NDIM) && g.has_shift;
+        if (twid) build_twiddles<kPoseThreads>(g, ip.sx, ip.sy, tw);
         const float2* V = rec + (long long)ir.r * g.rec_elems;
         const float2* VG =
             WIN == kGrouped ? grouped + (long long)ir.r * g.Dv * g.gplane * Taps<INTERP>::N : V;
@@ -436,7 +478,9 @@ __global__ void __launch_bounds__(kPoseThreads, 4) grad_pose_kernel(
         auto add = [&](int row, int kx, float2 v, const float2* dv) {
             const int ky = row_freq(row, g.Do, g.halfo, g.centered);
             float2 gp = __ldg(gy + row * g.Ho + kx);
-            if (g.has_shift)
+            if (twid)
+                gp = cmul_conj(gp, cmul(tw[kx], tw[g.Ho + row]));
+            else if (g.has_shift)
                 gp = cmul_conj(gp, shift_phase((float)kx, (float)ky, ip.sx, ip.sy, g.Do_f, g.inv_Do));
             accumulate_grad<NDIM>(acc, gp, v, dv, kx, ky);
         };
@@ -1916,7 +1960,7 @@ struct TableShape {
     long long n_work;
 };
 
-TableShape table_shape(const Geom& g, int sms, int ctas_per_sm, int threads = kThreads)
+TableShape table_shape(const Geom& g, int sms, int ctas_per_sm, int threads, int ndim)
 {
     const long long n_items = (long long)g.n_rec * g.n_pose;
     const long long max_parts = (g.img_elems + threads - 1) / threads;
@@ -1926,6 +1970,7 @@ TableShape table_shape(const Geom& g, int sms, int ctas_per_sm, int threads = kT
     const long long cap = 16LL * sms;  // persistent-style: the table is built once per CTA
     t.grid = (unsigned)(t.n_work < cap ? t.n_work : cap);
     t.smem = (size_t)(g.Do + 1 + kWarpQueue * (threads / 32)) * sizeof(int);  // table + warp queues
+    if (use_twiddles(g, ndim)) t.smem += 8 + 2 * (size_t)(g.Ho + g.Do) * sizeof(float2);  // aligned
     return t;
 }
 
@@ -1940,7 +1985,7 @@ void launch_project_table(const Geom& g, const float2* R, const float* rot, cons
                           float2* Y, const float2* grouped, int sms, cudaStream_t stream)
 {
     constexpr int BT = NDIM == 3 ? kFwd3Threads : kThreads;
-    const TableShape t = table_shape(g, sms, 4, BT);
+    const TableShape t = table_shape(g, sms, 4, BT, NDIM);
     project_kernel<NDIM, INTERP, WIN><<<t.grid, BT, t.smem, stream>>>(
         R, rot, shift, Y, g, t.splits, t.n_work, grouped);
 }
@@ -1970,7 +2015,7 @@ void launch_grad_table(const Geom& g, const float2* R, const float* rot, const f
                        const float2* G, float* grot, float* gsh, const float2* grouped, int sms,
                        cudaStream_t stream)
 {
-    const TableShape t = table_shape(g, sms, 4, kPoseThreads);
+    const TableShape t = table_shape(g, sms, 4, kPoseThreads, NDIM);
     grad_pose_kernel<NDIM, INTERP, WIN><<<t.grid, kPoseThreads, t.smem, stream>>>(
         R, rot, shift, G, grot, gsh, g, t.splits, t.n_work, grouped);
 }
