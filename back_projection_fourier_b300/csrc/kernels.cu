@@ -15,8 +15,15 @@
 // the volume in aligned vector windows or, with a workspace, from the grouped copy in one
 // aligned load; the others -- taps on the x = 0 plane or past x = Dv/2 -- are queued in
 // shared memory and evaluated densely with the exact per-tap rule, so they do not make whole
-// warps diverge.  The volume (and its grouped copy at D <= 128) stays L2-resident: a D = 256
-// half volume is 68 MB of a 126 MB L2.
+// warps diverge (with the grouped copy, whose rows also hold the mirrored taps left of x = 0,
+// only taps past x = Dv/2 and a few band-edge cases remain).  The volume (and its grouped copy
+// at D <= 128) stays L2-resident: a D = 256 half volume is 68 MB of a 126 MB L2.
+//
+// Scatter kernels (volume gradient, insertion).  3D cubic: scatter_tile_kernel, a warp per
+// 4 x 4 pixel tile with a private shared-memory box, lanes on a pixel's 64 taps; its POSE
+// instance is the one-pass backward.  3D linear: scatter_lane_kernel, a pixel per lane.  2D
+// cubic with weights: scatter_tile2d_kernel, a tile per half-warp.  Other 2D: the
+// owner-computes scatter_rows_kernel.  Boxes beyond the shared tables: backproject_kernel.
 #include "gather.cuh"
 #include "kernels.h"
 #include "scatter.cuh"
