@@ -100,6 +100,24 @@ def test_rot2d_d256_cubic_full_sampled_images():
     assert max_rel(host(g_sh[ti]), r_sh) <= TOL_BWD
 
 
+def test_rot2d_d256_cubic_insertion_with_weights_sampled_images():
+    """The 2D insertion with weights (the half-warp tile scatter) over the whole 2D workload:
+    every image has its own output image, so sampled images compare exactly with the oracle."""
+    wl = synth.make_workload("rot2d_d256_cubic_b8192")
+    R, S, G = dev(wl.rot), dev(wl.shift), dev(wl.grad)
+    rng = np.random.default_rng(5)
+    w = rng.uniform(0.1, 2.0, wl.grad.shape).astype(np.float32)
+    op = wl_opts(wl)
+    img, wimg = tp.backproject(G, R, S, dev(w), Dv=wl.D, opts=op, ndim=2)
+    idx = rng.choice(wl.B, 24, replace=False)
+    ti = torch.from_numpy(idx).cuda()
+    kw = oracle_kw(wl)
+    g_s, rot_s, sh_s, w_s = (np.ascontiguousarray(a[idx]) for a in (wl.grad, wl.rot, wl.shift, w))
+    r_img, r_w = oracle.backproject(2, g_s, rot_s, weights=w_s, shift=sh_s, Dv=wl.D, **kw)
+    assert max_rel(host(img[ti]), r_img) <= TOL_BWD
+    assert max_rel(host(wimg[ti]), r_w) <= TOL_BWD
+
+
 def _fwdbwd3d_sampled(name, n_pix=6000, n_poses=48, n_sub=None):
     """n_sub: None compares the whole volume gradient of the full batch with the oracle;
     an integer compares the whole volume gradient of the first n_sub poses of every
