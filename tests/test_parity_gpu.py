@@ -226,7 +226,7 @@ MIXED = [(ndim, n_rot, n_sh) for ndim in (3, 2) for n_rot, n_sh in ((3, 1), (1, 
 def test_mixed_pose_broadcast(ndim, n_rot, n_sh):
     """Rotations and shifts broadcast over the reconstructions independently (n_rot and n_sh
     each 1 or n_rec): every entry point, the gradient of the shared array summed over the
-    reconstructions, on the plain and the workspace calls."""
+    reconstructions, on the plain, the workspace and the one-pass calls."""
     rng = np.random.default_rng(40 + 10 * ndim + n_rot)
     n_rec, n_pose, D = 3, 9, 26
     H = D // 2 + 1
@@ -261,6 +261,11 @@ def test_mixed_pose_broadcast(ndim, n_rot, n_sh):
         assert max_rel(host(g1[0]), r_rec) <= TOL_BWD
         assert max_rel(host(g1[1]), r_rot) <= TOL_BWD
         assert max_rel(host(g1[2]), r_sh) <= TOL_BWD
+        # the one-pass backward: a shared pose's gradient gathers every reconstruction's terms
+        g2 = tp.project_backward(V, R, G, S, want_shift=True, opts=op, fused=True)
+        assert max_rel(host(g2[0]), r_rec) <= TOL_BWD
+        assert max_rel(host(g2[1]), r_rot) <= TOL_BWD
+        assert max_rel(host(g2[2]), r_sh) <= TOL_BWD
 
 
 def _bp_grads(case, with_weights, seed):
