@@ -83,3 +83,15 @@ def test_shared_atomic_context_of_the_linear_insertion():
     wc = synth.make_workload("insert3d_d128_b16384", B=16, interp=synth.CUBIC, with_grad=False)
     rc = bench.relevant_roofline(wc, {"insertion": 2.0}, hbm, 6400.0, pk, 2000.0)
     assert "smem_red_frac" not in rc["insertion"]
+
+
+def test_one_pass_backward_bytes_and_label():
+    """The one-pass backward reads the upstream gradient and the poses once, reads the volume
+    and writes its gradient: per projection 66 560 + 88 B, per launch twice the volume.  Its
+    step is labelled in the config that both arms share."""
+    wl = synth.make_workload(bench.DEFAULT_WORKLOAD, B=16, with_grad=False)
+    b = bench.hbm_bytes(wl)
+    vol = 128 * 128 * 65 * 8
+    assert b["backward_fused"] == 16 * (66560 + 88) + 2 * vol
+    assert "one-pass" in bench.workload_config(wl, "l2", True)["step"]
+    assert "one-pass" not in bench.workload_config(wl, "l2")["step"]
